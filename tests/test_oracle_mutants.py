@@ -1,0 +1,60 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case plants one mistake in a temporary copy of the oracle's C source
+(never in the oracle itself), builds it, and runs the oracle pin tests against
+that build; they must fail.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "zero_oracle.c")
+PIN_TESTS = ["tests/test_oracle_step.py", "tests/test_oracle_formats.py"]
+
+MUTANTS = {
+    "reduce-reverse-rank-order": ("for (int r = 0; r < nd; r++)\n            s = s +",
+                                  "for (int r = nd - 1; r >= 0; r--)\n            s = s +"),
+    "reduce-transposed-index": ("grads[(int64_t)r * rank_stride + i]", "grads[i * nd + r]"),
+    "reduce-no-average": ("float avg = s / (float)nd;", "float avg = s;"),
+    "reduce-no-unscale": ("float gi  = avg / loss_scale;", "float gi  = avg;"),
+    "adam-no-bias-correction-m": ("float mhat = mi / bc1;", "float mhat = mi;"),
+    "adam-eps-inside-sqrt": ("(sqrtf(vhat) + hp->eps)", "sqrtf(vhat + hp->eps)"),
+    "adam-v-of-g-not-g2": ("omb2 * (gi * gi)", "omb2 * gi"),
+    "adam-betas-swapped-in-m": ("hp->beta1 * m[i] + omb1 * gi", "hp->beta2 * m[i] + omb2 * gi"),
+    "adam-wrong-sign": ("p = p - hp->lr * upd;", "p = p + hp->lr * upd;"),
+    "adamw-decay-dropped": ("if (hp->decoupled_wd) p  = p * decay;",
+                            "if (hp->decoupled_wd) p  = p;"),
+    "bias-correction-stuck-at-t1": ("st->beta1_pow = st->beta1_pow * (double)hp->beta1;",
+                                    "st->beta1_pow = (double)hp->beta1;"),
+    "clip-always": ("if (clip > 0.0f && norm > (double)clip)", "if (clip > 0.0f)"),
+    "norm-squares-in-float": ("acc = acc + (double)g[i] * (double)g[i];",
+                              "acc = acc + (double)(g[i] * g[i]);"),
+    "skip-keeps-scale": ("st->loss_scale = st->loss_scale * hp->backoff;",
+                         "st->loss_scale = st->loss_scale;"),
+    "skip-advances-t": ("res->skipped  = 1;", "res->skipped  = 1; st->t = st->t + 1;"),
+    "round-ties-away": ("(frac == 0.5 && fmod(r, 2.0) != 0.0)", "(frac == 0.5)"),
+    "gather-off-by-one": ("out[j] = slices[k][j % slice];",
+                          "out[j] = slices[k][(j + 1) % slice];"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(tmp_path, name):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    mut = tmp_path / "zero_oracle.c"
+    mut.write_text(src.replace(old, new))
+    (tmp_path / "zero_oracle.h").write_text(open(SRC[:-1] + "h").read())
+    so = tmp_path / "libmutant.so"
+    sys.path.insert(0, ROOT)
+    import oracle
+    subprocess.run(["gcc", *oracle.CFLAGS, "-o", str(so), str(mut), "-lm"], check=True)
+    env = dict(os.environ, ZO_ORACLE_LIB=str(so))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        *PIN_TESTS], cwd=ROOT, env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
