@@ -1,0 +1,430 @@
+#!/usr/bin/env python3
+"""Benchmark of the ZeRO-DP sharded mixed-precision optimizer step on GB300.
+
+Workload: the GPT-2 1.5B parameter list (48 layers, h 1600, ffn 6400, vocab
+50257, ctx 1024: 1,557,611,200 parameters), Nd = 16 emulated data-parallel
+ranks, ZeRO-2, fp16 gradients N(0, 1e-3) x 65536 under dynamic loss scaling,
+clip by global norm 1.0, Adam (lr 1e-3, betas 0.9/0.999, eps 1e-8).  Synthetic
+seeded inputs; no weights or data.
+
+One step = one zero_step call: the 16-way fixed-order reduce-scatter and
+average, unscale + overflow flag, global norm, clip, Adam on the fp32 master,
+m and v, the fp16 cast and the write-back of every shard into the flat
+parameter buffer.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  For N > 1 (torchrun), every rank runs its own
+independent replica of the workload on its own GPU (the path has no data
+exchange between GPUs here): weak scaling, barrier + max-over-ranks timing.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sharded Adam step params/s and HBM GB/s vs GB300 peak (GPT-2 1.5B, Nd=16)"
+NOMINAL_HBM_GBS = 7900.0
+FALLBACK_HBM_GBS = 6800.0
+STATUS_BYTES = 72            # the optimizer scalars + step status zero_step_result copies
+
+
+# --------------------------------------------------------------- distributed
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+    rank, local, ws = dist_env()
+    if ws > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend, rank=rank, world_size=ws)
+    return rank, local, ws
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def reduce_scalar(x: float, op: str, device=None) -> float:
+    """max or sum of one float over ranks (timing bookkeeping only)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64,
+                     device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------- helpers
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def host_mem_available() -> int:
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) of the SM clock and throttle reasons."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.window = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            rows.append((ts, parts))
+        if not rows:
+            return None
+        t0, t1 = self.window if self.window else (rows[0][0], rows[-1][0])
+        inside = [p for ts, p in rows if t0 - 0.25 <= ts <= t1 + 0.25] or [p for _, p in rows]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+        sm = [num(p[2]) for p in inside if not math.isnan(num(p[2]))]
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for p in inside:
+            for name, val in zip(names, p[6:10]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(inside[0][3]), "reasons": sorted(reasons),
+                "samples": len(inside),
+                "power_w_max": max((num(p[4]) for p in inside), default=None)}
+
+
+# ----------------------------------------------------------------- workload
+def workload():
+    from gen import workloads
+    return workloads.gpt2_xl()
+
+
+def config_of(w, padded):
+    return {"workload": f"{w.name}: GPT-2 1.5B parameter list (48 layers, h=1600, ffn=6400, "
+                        f"vocab 50257, ctx 1024), {len(w.shapes)} tensors",
+            "psi": w.psi, "nd": w.nd, "zero_stage": w.stage, "padded_elems": padded,
+            "grads": "fp16 N(0,1e-3) x 65536 loss scale (dynamic)", "clip_norm": w.clip,
+            "optimizer": "Adam lr 1e-3 betas (0.9, 0.999) eps 1e-8",
+            "l2": "inputs (~78 GB resident) far larger than the 129 MB L2; no flush needed",
+            "parallelism": "Nd ranks emulated in one GPU's HBM"}
+
+
+# ----------------------------------------------------------- CPU baseline
+def oracle_sample(w, n_sample: int, threads: int, repeats_min_s: float = 0.0, max_repeats=1):
+    """Time the oracle (as it stands) on the first n_sample elements of the flat
+    vector with all Nd ranks' contributions; returns (params/s, seconds/step, reps)."""
+    import numpy as np
+    import gen
+    import oracle
+    g = gen.ranks_16(w.seed, gen.STREAM_GRAD, 1, w.nd, n_sample, w.grad_sigma, w.loss_scale,
+                     w.dtype)
+    master0 = gen.f32(w.seed, gen.STREAM_MASTER, 0, 0, n_sample, w.master_sigma)
+    opt = oracle.Opt(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps,
+                     weight_decay=w.weight_decay, decoupled_wd=w.decoupled_wd,
+                     clip_norm=w.clip, dynamic_scale=w.dynamic_scale, backoff=0.5,
+                     growth_interval=1000)
+    master, m, v = master0.copy(), np.zeros(n_sample, np.float32), np.zeros(n_sample, np.float32)
+    params = np.zeros(n_sample, np.uint16)
+    st = oracle.new_scalars(w.loss_scale)
+    shard = oracle.shard_elems(n_sample, w.nd)
+    times = []
+    t_start = time.perf_counter()
+    while True:
+        t0 = time.perf_counter()
+        oracle.step_sharded(w.nd, w.dtype, g, master, m, v, params, opt, st, shard=shard,
+                            nthreads=threads)
+        times.append(time.perf_counter() - t0)
+        if len(times) >= max_repeats or time.perf_counter() - t_start >= repeats_min_s:
+            break
+    per_step = sum(times) / len(times)
+    return n_sample / per_step, per_step, len(times)
+
+
+def oracle_threads(nd: int) -> int:
+    return max(1, min(os.cpu_count() or 1, nd))
+
+
+# ------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    import gen
+    import zero_sharded_mixed_02_gb300 as z
+    from zero_sharded_mixed_02_gb300 import build as zbuild
+
+    rank, local, ws = dist_init("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    zbuild.build()
+    w = workload()
+    hp = z.hparams(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
+                   decoupled_wd=w.decoupled_wd, clip_norm=w.clip, loss_scale=w.loss_scale,
+                   dynamic_scale=w.dynamic_scale, backoff=0.5, growth_interval=1000)
+    plan = z.zero_plan_create(w.psi, w.nd, w.stage, w.dtype, w.shapes, hp)
+    shard, padded, _, ws_bytes = z.zero_plan_layout(plan)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+
+    grads = torch.empty((w.nd, padded), dtype=torch.int16, device=dev)
+    master = torch.zeros(padded, dtype=torch.float32, device=dev)
+    m = torch.zeros(padded, dtype=torch.float32, device=dev)
+    v = torch.zeros(padded, dtype=torch.float32, device=dev)
+    params = torch.zeros(padded, dtype=torch.int16, device=dev)
+    work = torch.empty(max(ws_bytes, 16) // 4, dtype=torch.float32, device=dev)
+    gen.cuda_ranks_16(grads.data_ptr(), w.seed, gen.STREAM_GRAD, 1, w.nd, w.psi, w.grad_sigma,
+                      w.loss_scale, w.dtype, rank_stride=padded, cuda_stream=sp)
+    gen.cuda_f32(master.data_ptr(), w.seed, gen.STREAM_MASTER, 0, 0, w.psi, w.master_sigma,
+                 cuda_stream=sp)
+    torch.cuda.synchronize(dev)
+
+    def step():
+        z.zero_step(plan, grads, master, m, v, params, work, sp)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    warm = z.zero_step_result(plan)
+
+    # ---- device-timed region: K steps, inputs resident in HBM ----
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.5)
+    z.zero_plan_profile(plan, 1)
+    launches0 = z.zero_plan_kernel_times(plan)["launches"]
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dev)
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    barrier(dev)
+    sampler.mark(t_wall0, t_wall1)
+    ms_local = ev0.elapsed_time(ev1)
+    kt = z.zero_plan_kernel_times(plan)
+    z.zero_plan_profile(plan, 0)
+    clocks = sampler.stop()
+    ms_total = reduce_scalar(ms_local, "max", dev)
+    res = z.zero_step_result(plan)
+
+    psi, nd, K = w.psi, w.nd, args.steps
+    ms_step = ms_total / K
+    value = psi * K * ws / (ms_total / 1e3)
+    peak, peak_kind = measured_peaks()
+    roof_bytes = (2 * nd + 26) * psi
+    floor_bytes = (2 * nd + 34) * psi
+    step_gbs = roof_bytes / (ms_step / 1e3) / 1e9
+    launches = kt["launches"] - launches0
+
+    # dominant kernel: the pass with more device time
+    a_ms = kt["reduce_ms"] / max(kt["steps"], 1)
+    b_ms = kt["update_ms"] / max(kt["steps"], 1)
+    if a_ms >= b_ms:
+        kname, kms, kbytes = "k_reduce (fold + unscale + flag + norm partials, writes fp32 g)", \
+            a_ms, (2 * nd + 4) * psi
+    else:
+        kname, kms, kbytes = "k_update (clip + Adam + cast + write-back)", b_ms, 30 * psi
+    achieved = kbytes / (kms / 1e3) / 1e9
+
+    out = {
+        "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded counter-based generator; GPT-2 1.5B shape list, no weights)",
+        "config": config_of(w, padded),
+        "hbm_gbs_roofline_bytes": step_gbs,
+        "roofline_bytes_per_elem": 2 * nd + 26,
+        "frac_of_measured_hbm": step_gbs / peak,
+        "frac_of_nominal_hbm": step_gbs / NOMINAL_HBM_GBS,
+        "hbm_gbs_floor_bytes": floor_bytes / (ms_step / 1e3) / 1e9,
+        "floor_bytes_per_elem": 2 * nd + 34,
+        "kernel_ms": {"reduce": a_ms, "update": b_ms},
+        "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak,
+                     "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind ==
+                     "measured" else "fallback", "unit": "GB/s", "frac": achieved / peak,
+                     "algorithmic_bytes_per_launch": kbytes, "traffic": None},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "step_result": {k: res[k] for k in ("skipped", "grad_norm", "clip_coef", "loss_scale",
+                                            "t")},
+        "warmup_result": {"t": warm["t"], "grad_norm": warm["grad_norm"]},
+    }
+
+    # ---- end to end through the C ABI: host gradients copied in every step ----
+    if not args.no_e2e:
+        out["e2e"] = e2e_leg(args, z, plan, w, grads, master, m, v, params, work, dev, stream)
+
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only) ----
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        n_s = args.cpu_sample
+        thr = oracle_threads(nd)
+        pps, per, reps = oracle_sample(w, n_s, thr, repeats_min_s=10.0, max_repeats=50)
+        out["cpu_baseline"] = {
+            "value": pps, "unit": "params/s", "cores": thr, "kind": "oracle",
+            "sample": f"first {n_s} elements of the flat vector x {nd} ranks' fp16 gradients, "
+                      f"one full oracle step each ({reps} steps, {per:.3f} s/step)"}
+
+    z.zero_plan_destroy(plan)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def e2e_leg(args, z, plan, w, grads, master, m, v, params, work, dev, stream):
+    """Same metric through the public API with host-resident gradients: every
+    step copies the 16 ranks' fp16 gradients from pinned host memory to the
+    device, runs zero_step and reads the step status back."""
+    import torch
+    nbytes = grads.numel() * 2
+    avail = host_mem_available()
+    if avail and avail < nbytes + (8 << 30):
+        return {"value": None, "unit": "params/s", "h2d_bytes_per_step": nbytes,
+                "d2h_bytes_per_step": STATUS_BYTES,
+                "skipped": f"host has {avail / 1e9:.0f} GB available, needs {nbytes / 1e9:.0f} GB "
+                           "pinned"}
+    host = torch.empty(grads.shape, dtype=grads.dtype, pin_memory=True)
+    host.copy_(grads)
+    sp = stream.cuda_stream
+    K = max(3, min(args.steps, args.e2e_steps))
+    for _ in range(2):
+        grads.copy_(host, non_blocking=True)
+        z.zero_step(plan, grads, master, m, v, params, work, sp)
+        z.zero_step_result(plan)
+    barrier(dev)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(K):
+        grads.copy_(host, non_blocking=True)
+        z.zero_step(plan, grads, master, m, v, params, work, sp)
+        z.zero_step_result(plan)
+    torch.cuda.synchronize(dev)
+    dt = reduce_scalar(time.perf_counter() - t0, "max", dev)
+    _, _, ws = dist_env()
+    del host
+    return {"value": w.psi * K * ws / dt, "unit": "params/s", "h2d_bytes_per_step": nbytes,
+            "d2h_bytes_per_step": STATUS_BYTES, "steps": K, "ms_per_step": dt / K * 1e3}
+
+
+# ------------------------------------------------------------ reference arm
+def run_reference(args):
+    """The CPU oracle, as it stands, on the host cores: each step is one oracle
+    step over a bounded sample of the same workload."""
+    rank, _, ws = dist_env()
+    if rank != 0:
+        return
+    w = workload()
+    thr = oracle_threads(w.nd)
+    n_s = args.ref_sample
+    import oracle
+    padded = oracle.shard_elems(w.psi, w.nd) * w.nd
+    oracle_sample(w, n_s, thr, max_repeats=max(1, args.warmup))          # warm-up
+    pps, per, reps = oracle_sample(w, n_s, thr, max_repeats=args.steps)
+    out = {
+        "impl": "reference", "metric": METRIC, "value": pps, "unit": "params/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded counter-based generator; GPT-2 1.5B shape list, no weights)",
+        "config": config_of(w, padded),
+        "cpu_baseline": {"value": pps, "unit": "params/s", "cores": thr, "kind": "oracle",
+                         "sample": f"first {n_s} elements x {w.nd} ranks per step"},
+        "e2e": {"value": pps, "unit": "params/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample", type=int, default=1 << 23)
+    ap.add_argument("--ref-sample", type=int, default=1 << 21)
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)          # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,229 @@
+"""Parity harness: the same seeded inputs through the CPU oracle and through the
+CUDA library's C ABI, and the comparison rules.
+
+Tolerances (GPU vs oracle):
+  reduced gradient, overflow flags, skip decisions, t, loss scale: bit-exact
+  fp32 master, m, v: relative error <= 1e-6, with rel(a, b) = 0 when a and b
+      are the same bits, else |a - b| / max(|a|, |b|)
+  16-bit parameters: <= 1 unit in the last place (ordered-integer distance)
+  grad norm: relative error <= 1e-5
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import List, Optional
+
+import numpy as np
+
+import gen
+import oracle
+
+REL_STATE = 1e-6
+REL_NORM = 1e-5
+ULP_PARAM = 1
+
+
+# ---------------------------------------------------------------- comparisons
+def rel_err(a: np.ndarray, b: np.ndarray) -> float:
+    a = np.ascontiguousarray(a, np.float32)
+    b = np.ascontiguousarray(b, np.float32)
+    if a.size == 0:
+        return 0.0
+    same = a.view(np.uint32) == b.view(np.uint32)
+    a64, b64 = a.astype(np.float64), b.astype(np.float64)
+    den = np.maximum(np.abs(a64), np.abs(b64))
+    with np.errstate(invalid="ignore", divide="ignore"):
+        r = np.abs(a64 - b64) / np.where(den == 0, 1.0, den)
+    r = np.where(same, 0.0, r)
+    r = np.where(np.isnan(r), np.inf, r)
+    return float(r.max())
+
+
+def ulp16(a: np.ndarray, b: np.ndarray) -> int:
+    def key(x):
+        x = np.asarray(x, np.uint16).astype(np.int32)
+        mag = x & 0x7FFF
+        return np.where(x & 0x8000, -mag, mag)
+    if np.asarray(a).size == 0:
+        return 0
+    return int(np.abs(key(a) - key(b)).max())
+
+
+def assert_state_close(gpu, ora, what=""):
+    for name, x, y in zip(("master", "m", "v"), gpu[:3], ora[:3]):
+        e = rel_err(x, y)
+        assert e <= REL_STATE, f"{what} {name}: max rel err {e:.3g}"
+    u = ulp16(gpu[3], ora[3])
+    assert u <= ULP_PARAM, f"{what} params: {u} ulp"
+
+
+# ------------------------------------------------------------------ inputs
+@dataclasses.dataclass
+class Case:
+    shapes: list
+    nd: int
+    stage: int = 2
+    dtype: int = gen.BF16
+    grad_sigma: float = 1e-2
+    loss_scale: float = 1.0
+    dynamic_scale: int = 0
+    clip: float = 0.0
+    lr: float = 1e-3
+    weight_decay: float = 0.0
+    decoupled_wd: int = 1
+    steps: int = 2
+    inf_steps: tuple = ()
+    nan_steps: tuple = ()
+    units: Optional[List[int]] = None
+    seed: int = 0
+    growth_interval: int = 1000
+
+    @property
+    def psi(self):
+        return int(sum(int(np.prod(s)) for s in self.shapes))
+
+    def opt(self):
+        return oracle.Opt(lr=self.lr, weight_decay=self.weight_decay,
+                          decoupled_wd=self.decoupled_wd, clip_norm=self.clip,
+                          dynamic_scale=self.dynamic_scale, backoff=0.5,
+                          growth_interval=self.growth_interval)
+
+    def hparams(self, z):
+        return z.hparams(lr=self.lr, weight_decay=self.weight_decay,
+                         decoupled_wd=self.decoupled_wd, clip_norm=self.clip,
+                         loss_scale=self.loss_scale, dynamic_scale=self.dynamic_scale,
+                         backoff=0.5, growth_interval=self.growth_interval)
+
+
+def from_workload(w, **over) -> Case:
+    c = Case(shapes=list(w.shapes), nd=w.nd, stage=w.stage, dtype=w.dtype,
+             grad_sigma=w.grad_sigma, loss_scale=w.loss_scale, dynamic_scale=w.dynamic_scale,
+             clip=w.clip, lr=w.lr, weight_decay=w.weight_decay, decoupled_wd=w.decoupled_wd,
+             steps=w.steps, inf_steps=tuple(w.inf_steps), units=w.units, seed=w.seed)
+    return dataclasses.replace(c, **over)
+
+
+def grads_for_step(c: Case, step: int, n: int, rank_stride: int, scale: float,
+                   valid_mask: Optional[np.ndarray] = None) -> np.ndarray:
+    """[nd][rank_stride] 16-bit gradients of step `step` (1-based), generated with
+    the loss scale in force; +inf / NaN planted on the overflow steps."""
+    g = gen.ranks_16(c.seed, gen.STREAM_GRAD, step, c.nd, n, c.grad_sigma, scale, c.dtype,
+                     rank_stride=rank_stride)
+    if valid_mask is not None:
+        g[:, :n][:, ~valid_mask] = 0
+    for steps, bits in ((c.inf_steps, 0x7C00 if c.dtype == gen.FP16 else 0x7F80),
+                        (c.nan_steps, 0x7E00 if c.dtype == gen.FP16 else 0x7FC0)):
+        if step in steps:
+            r, i = gen.inf_site(c.seed, step, n, c.nd)
+            if valid_mask is not None:
+                i = int(np.flatnonzero(valid_mask)[i % int(valid_mask.sum())])
+            g[r, i] = bits
+    return g
+
+
+# ------------------------------------------------------------------- runs
+@dataclasses.dataclass
+class Run:
+    master: np.ndarray
+    m: np.ndarray
+    v: np.ndarray
+    params: np.ndarray
+    results: list
+    g32: Optional[np.ndarray] = None
+
+
+def stage3_valid_mask(z, plan, nd, rank=0):
+    """positions of one rank's shard that hold real (not padding) elements"""
+    _, total, nunits, _ = z.zero_plan_layout(plan)
+    mask = np.zeros(total, bool)
+    for u in range(nunits):
+        ln, sl, off = z.zero_plan_unit(plan, u)
+        valid = max(0, min(sl, ln - rank * sl))
+        mask[off:off + valid] = True
+    return mask
+
+
+def run_gpu(z, c: Case, keep_g32=False, plan_out=None) -> Run:
+    import torch
+    dev = torch.device("cuda", 0)
+    plan = z.zero_plan_create(c.psi, c.nd, c.stage, c.dtype, c.shapes, c.hparams(z),
+                              units=c.units if c.stage == 3 else None)
+    try:
+        shard, padded, nunits, ws = z.zero_plan_layout(plan)
+        n = c.psi if c.stage <= 2 else padded
+        mask = stage3_valid_mask(z, plan, c.nd) if c.stage == 3 else None
+        master0 = gen.f32(c.seed, gen.STREAM_MASTER, 0, 0, n, 0.02)
+        if mask is not None:
+            master0[~mask] = 0
+        master = torch.zeros(padded, dtype=torch.float32, device=dev)
+        master[:n] = torch.from_numpy(master0).to(dev)
+        m = torch.zeros(padded, dtype=torch.float32, device=dev)
+        v = torch.zeros(padded, dtype=torch.float32, device=dev)
+        params = torch.zeros(padded, dtype=torch.int16, device=dev)
+        work = torch.empty(max(ws, 16) // 4, dtype=torch.float32, device=dev) if ws else None
+        grads = torch.empty((c.nd, padded), dtype=torch.int16, device=dev)
+        stream = torch.cuda.current_stream().cuda_stream
+        results = []
+        scale = c.loss_scale
+        for step in range(1, c.steps + 1):
+            g = grads_for_step(c, step, n, padded, scale, mask)
+            grads.copy_(torch.from_numpy(g.view(np.int16)))
+            z.zero_step(plan, grads, master, m, v, params, work, stream)
+            r = z.zero_step_result(plan)
+            r["overflow"] = z.zero_step_overflow(plan)
+            results.append(r)
+            scale = r["loss_scale"]
+        torch.cuda.synchronize()
+        out = Run(master[:n].cpu().numpy(), m[:n].cpu().numpy(), v[:n].cpu().numpy(),
+                  params[:n].cpu().numpy().view(np.uint16), results)
+        if keep_g32 and work is not None:
+            out.g32 = work[:n].cpu().numpy()
+        if plan_out is not None:
+            plan_out.append(plan)
+            plan = None
+        return out
+    finally:
+        if plan is not None:
+            z.zero_plan_destroy(plan)
+
+
+def run_oracle(c: Case, n: int, padded: int, mask=None, sharded_threads=0) -> Run:
+    master = gen.f32(c.seed, gen.STREAM_MASTER, 0, 0, n, 0.02)
+    if mask is not None:
+        master[~mask] = 0
+    m = np.zeros(n, np.float32)
+    v = np.zeros(n, np.float32)
+    params = np.zeros(n, np.uint16)
+    st = oracle.new_scalars(c.loss_scale)
+    opt = c.opt()
+    results = []
+    for step in range(1, c.steps + 1):
+        g = grads_for_step(c, step, n, padded, st.loss_scale, mask)
+        g = np.ascontiguousarray(g[:, :n])
+        if sharded_threads:
+            r = oracle.step_sharded(c.nd, c.dtype, g, master, m, v, params, opt, st,
+                                    nthreads=sharded_threads)
+        else:
+            r = oracle.step(c.nd, c.dtype, g, master, m, v, params, opt, st)
+        r["loss_scale"] = st.loss_scale
+        r["t"] = st.t
+        results.append(r)
+    return Run(master, m, v, params, results)
+
+
+def compare_runs(gpu: Run, ora: Run, what=""):
+    assert len(gpu.results) == len(ora.results)
+    for k, (a, b) in enumerate(zip(gpu.results, ora.results), start=1):
+        assert a["skipped"] == b["skipped"], f"{what} step {k}: skip {a} vs {b}"
+        assert a["overflow"] == b["overflow"], f"{what} step {k}: overflow {a} vs {b}"
+        assert a["t"] == b["t"] and a["loss_scale"] == b["loss_scale"], f"{what} step {k}"
+        if np.isfinite(b["grad_norm"]):
+            e = abs(a["grad_norm"] - b["grad_norm"]) / max(abs(b["grad_norm"]), 1e-300)
+            assert e <= REL_NORM, f"{what} step {k}: norm {a['grad_norm']} vs {b['grad_norm']}"
+            if not a["skipped"]:
+                ce = abs(a["clip_coef"] - b["clip_coef"]) / max(abs(b["clip_coef"]), 1e-30)
+                assert ce <= 4e-7, f"{what} step {k}: clip {a['clip_coef']} vs {b['clip_coef']}"
+        else:
+            assert not np.isfinite(a["grad_norm"])
+    assert_state_close((gpu.master, gpu.m, gpu.v, gpu.params),
+                       (ora.master, ora.m, ora.v, ora.params), what)

@@ -1,0 +1,229 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle on the
+same seeded inputs, at sizes the oracle finishes in seconds that still span many
+blocks and a ragged tail.  Tolerances are in tests/harness.py."""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import gen
+import harness as H
+import oracle
+from gen import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def z():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from zero_sharded_mixed_02_gb300 import build
+    build.build()
+    import zero_sharded_mixed_02_gb300 as z
+    z.lib()
+    return z
+
+
+def check(z, c, bit_exact=False, g32=False):
+    gpu = H.run_gpu(z, c, keep_g32=g32)
+    n = gpu.master.size
+    padded = n
+    if c.stage <= 2:
+        plan = z.zero_plan_create(c.psi, c.nd, c.stage, c.dtype, c.shapes, c.hparams(z))
+        padded = z.zero_plan_layout(plan)[1]
+        z.zero_plan_destroy(plan)
+        mask = None
+    else:
+        plan = z.zero_plan_create(c.psi, c.nd, 3, c.dtype, c.shapes, c.hparams(z), units=c.units)
+        mask = H.stage3_valid_mask(z, plan, c.nd)
+        z.zero_plan_destroy(plan)
+    ora = H.run_oracle(c, n, padded, mask)
+    H.compare_runs(gpu, ora, what=f"psi={c.psi} nd={c.nd}")
+    if bit_exact:
+        for a, b in zip((gpu.master, gpu.m, gpu.v, gpu.params), (ora.master, ora.m, ora.v, ora.params)):
+            assert np.array_equal(a.view(np.uint32 if a.dtype == np.float32 else np.uint16),
+                                  b.view(np.uint32 if b.dtype == np.float32 else np.uint16))
+    if g32:
+        # the reduced (averaged, unscaled) gradient of the last step is bit-exact
+        last = c.steps
+        scale = gpu.results[-2]["loss_scale"] if c.steps > 1 else c.loss_scale
+        g = H.grads_for_step(c, last, n, padded, scale, mask)
+        want, _ = oracle.reduce(c.nd, c.dtype, np.ascontiguousarray(g[:, :n]), loss_scale=scale)
+        assert np.array_equal(gpu.g32.view(np.uint32), want.view(np.uint32))
+    return gpu, ora
+
+
+def test_tiny_flat_model(z):
+    # tiny flat model: 4 tensors, Nd=4, ZeRO-2, fp16 x1024 dynamic loss scale, 3 steps
+    c = H.from_workload(W.tiny())
+    gpu, ora = check(z, c, bit_exact=True, g32=True)
+    assert [r["t"] for r in gpu.results] == [1, 2, 3]
+
+
+def test_gpt2_small_family(z):
+    # GPT-2 small's settings (Nd=8, ZeRO-1, bf16, AdamW 0.01, clip 1.0, 10 steps)
+    # on a 2-layer model of the same shape family
+    w = W.scaled_gpt2(2, 256, 1024, 1000, 128, 8, W.gpt2_small())
+    c = H.from_workload(w)
+    gpu, _ = check(z, c, g32=True)
+    assert all(r["clip_coef"] < 1.0 for r in gpu.results)      # the clip is active
+
+
+def test_gpt2_xl_family_with_overflow(z):
+    # GPT-2 1.5B's settings (Nd=16, ZeRO-2, fp16 x65536 dynamic, clip 1, inf on
+    # steps 3 and 7: skipped, scale halved) on a 2-layer model of the same family
+    w = W.scaled_gpt2(2, 320, 1280, 3000, 256, 16, W.gpt2_xl())
+    c = H.from_workload(w)
+    gpu, _ = check(z, c, g32=True)
+    skipped = [r["skipped"] for r in gpu.results]
+    assert skipped == [0, 0, 1, 0, 0, 0, 1, 0, 0, 0]
+    assert gpu.results[-1]["loss_scale"] == 16384.0 and gpu.results[-1]["t"] == 8
+
+
+def test_llama_family_stage3_and_gather(z):
+    # LLaMA-3-8B's settings (Nd=64, ZeRO-3, bf16): rank 0's shard updated, then
+    # every unit gathered from 64 shards (rank 0's updated one + 63 seeded)
+    import torch
+    w = W.scaled_llama(2, 256, 512, 8, 2, 1000, 64, W.llama3_8b())
+    c = H.from_workload(w, steps=2)
+    plans = []
+    gpu = H.run_gpu(z, c, plan_out=plans)
+    plan = plans[0]
+    try:
+        _, total, nunits, _ = z.zero_plan_layout(plan)
+        assert nunits == 4
+        mask = H.stage3_valid_mask(z, plan, c.nd)
+        ora = H.run_oracle(c, total, total, mask)
+        H.compare_runs(gpu, ora, "stage3")
+        dev = torch.device("cuda", 0)
+        shards = [torch.from_numpy(gpu.params.view(np.int16)).to(dev)]
+        host_shards = [gpu.params]
+        for k in range(1, c.nd):
+            s = gen.s16(c.seed, gen.STREAM_SHARD, 0, k, total, 0.02, 1.0, c.dtype)
+            s[~H.stage3_valid_mask(z, plan, c.nd, rank=k)] = 0
+            host_shards.append(s)
+            shards.append(torch.from_numpy(s.view(np.int16)).to(dev))
+        for u in range(nunits):
+            ln, sl, off = z.zero_plan_unit(plan, u)
+            out = torch.full((ln + 8,), -1, dtype=torch.int16, device=dev)
+            z.zero_gather_layer(plan, u, shards, out, torch.cuda.current_stream().cuda_stream)
+            torch.cuda.synchronize()
+            got = out.cpu().numpy().view(np.uint16)
+            want = oracle.gather_unit(c.nd, ln, sl, [s[off:off + sl] for s in host_shards])
+            assert np.array_equal(got[:ln], want)
+            assert np.all(got[ln:] == 0xFFFF)                     # nothing past the unit
+    finally:
+        z.zero_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("nd", [1, 2, 8, 32])
+def test_bandwidth_sweep_point(z, nd):
+    # the sweep's flat bf16 model (no clip, no loss scale: the fused single pass),
+    # 5 warm-up steps + 1; every output bit-exact
+    c = H.Case(shapes=[(1 << 20,)], nd=nd, steps=6)
+    check(z, c, bit_exact=True)
+
+
+EDGE = []
+for psi in (1, 5, 13, 16, 4099, 65539):
+    for nd in (1, 2, 3, 5, 8, 16):
+        EDGE.append((psi, nd))
+
+
+@pytest.mark.parametrize("psi,nd", EDGE)
+@pytest.mark.parametrize("mode", ["fused", "clip", "fp16-dyn"])
+def test_edge_sizes(z, psi, nd, mode):
+    shapes = [(psi,)] if psi < 100 else [(psi - 7,), (7,)]
+    if mode == "fused":
+        c = H.Case(shapes=shapes, nd=nd, steps=3, weight_decay=0.01, decoupled_wd=0)
+    elif mode == "clip":
+        c = H.Case(shapes=shapes, nd=nd, steps=3, clip=0.05, weight_decay=0.01)
+    else:
+        c = H.Case(shapes=shapes, nd=nd, steps=4, dtype=gen.FP16, grad_sigma=1e-3,
+                   loss_scale=4096.0, dynamic_scale=1, inf_steps=(2,), growth_interval=2)
+    check(z, c, bit_exact=(mode != "clip"), g32=(mode != "fused" and nd >= 4))
+
+
+def test_nan_and_inf_skip_and_scale_schedule(z):
+    c = H.Case(shapes=[(3000,), (1000,)], nd=4, dtype=gen.FP16, grad_sigma=1e-3,
+               loss_scale=1024.0, dynamic_scale=1, steps=7, inf_steps=(2,), nan_steps=(5,),
+               growth_interval=2)
+    gpu, _ = check(z, c, bit_exact=True)
+    assert [r["skipped"] for r in gpu.results] == [0, 1, 0, 0, 1, 0, 0]
+    assert [r["loss_scale"] for r in gpu.results] == [1024, 512, 512, 1024, 512, 512, 1024]
+
+
+def test_static_scale_reports_overflow(z):
+    c = H.Case(shapes=[(5000,)], nd=4, dtype=gen.FP16, grad_sigma=1e-3, loss_scale=8.0,
+               steps=2, inf_steps=(2,), clip=1.0)
+    gpu = H.run_gpu(z, c)
+    assert [r["overflow"] for r in gpu.results] == [0, 1]
+    assert [r["skipped"] for r in gpu.results] == [0, 0]
+    assert gpu.results[-1]["t"] == 2
+
+
+def test_empty_model(z):
+    plan = z.zero_plan_create(0, 4, 2, 1, [], z.hparams())
+    try:
+        for _ in range(3):
+            z.zero_step(plan, None, None, None, None, None, None, 0)
+        r = z.zero_step_result(plan)
+        assert r["t"] == 3 and r["grad_norm"] == 0.0 and r["skipped"] == 0
+    finally:
+        z.zero_plan_destroy(plan)
+
+
+def test_deterministic_rerun(z):
+    c = H.Case(shapes=[(300_001,)], nd=8, clip=0.5, steps=3)
+    a = H.run_gpu(z, c)
+    b = H.run_gpu(z, c)
+    for x, y in zip((a.master, a.m, a.v, a.params), (b.master, b.m, b.v, b.params)):
+        assert x.tobytes() == y.tobytes()
+    assert [r["grad_norm"] for r in a.results] == [r["grad_norm"] for r in b.results]
+
+
+def test_misaligned_and_missing_pointers_rejected(z):
+    import torch
+    c = H.Case(shapes=[(4096,)], nd=4, clip=1.0)
+    plan = z.zero_plan_create(c.psi, c.nd, 2, c.dtype, c.shapes, c.hparams(z))
+    try:
+        _, padded, _, ws = z.zero_plan_layout(plan)
+        dev = torch.device("cuda", 0)
+        g = torch.zeros((4, padded), dtype=torch.int16, device=dev)
+        f = [torch.zeros(padded + 4, dtype=torch.float32, device=dev) for _ in range(3)]
+        p = torch.zeros(padded, dtype=torch.int16, device=dev)
+        w = torch.zeros(ws // 4, dtype=torch.float32, device=dev)
+        with pytest.raises(z.ZeroError):
+            z.zero_step(plan, g.data_ptr() + 2, f[0], f[1], f[2], p, w)
+        with pytest.raises(z.ZeroError):
+            z.zero_step(plan, g, f[0].data_ptr() + 4, f[1], f[2], p, w)
+        with pytest.raises(z.ZeroError):
+            z.zero_step(plan, g, f[0], f[1], f[2], p, None)         # workspace needed
+        z.zero_step(plan, g, f[0], f[1], f[2], p, w)
+        assert z.zero_step_result(plan)["t"] == 1
+    finally:
+        z.zero_plan_destroy(plan)
+
+
+def test_profile_counts_kernels(z):
+    import torch
+    c = H.Case(shapes=[(100_000,)], nd=8, clip=1.0, steps=1)
+    plan = z.zero_plan_create(c.psi, c.nd, 2, c.dtype, c.shapes, c.hparams(z))
+    try:
+        _, padded, _, ws = z.zero_plan_layout(plan)
+        dev = torch.device("cuda", 0)
+        g = torch.zeros((8, padded), dtype=torch.int16, device=dev)
+        f = [torch.zeros(padded, dtype=torch.float32, device=dev) for _ in range(3)]
+        p = torch.zeros(padded, dtype=torch.int16, device=dev)
+        w = torch.zeros(ws // 4, dtype=torch.float32, device=dev)
+        z.zero_plan_profile(plan, 1)
+        for _ in range(300):                                  # more than the event ring
+            z.zero_step(plan, g, f[0], f[1], f[2], p, w)
+        t = z.zero_plan_kernel_times(plan)
+        assert t["steps"] == 300 and t["launches"] == 600
+        assert t["reduce_ms"] > 0 and t["update_ms"] > 0
+        assert z.zero_plan_path(plan) == z.PATH_G32
+    finally:
+        z.zero_plan_destroy(plan)

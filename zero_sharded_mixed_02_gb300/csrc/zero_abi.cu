@@ -1,0 +1,564 @@
+// zero_abi.cu -- plans, validation, kernel dispatch and the extern "C" entry
+// points of libzero_b200 (declared and documented in include/zero_b200.h).
+#include <algorithm>
+#include <array>
+#include <cmath>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "zero_b200.h"
+#include "zero_launch.h"
+
+using namespace zero;
+
+namespace {
+
+constexpr int PATH_FUSED = 0, PATH_G32 = 1, PATH_RECOMPUTE = 2;
+constexpr int PROFILE_RING = 256;
+constexpr uint64_t LAYOUT_ALIGN = 64;   // elements; keeps 16-byte vectors inside a shard
+
+struct ProfileSlot {
+    cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+    bool used = false;
+};
+
+}  // namespace
+
+struct zero_plan {
+    uint64_t psi = 0;
+    int nd = 1, stage = 0;
+    zero_dtype_t dtype = ZERO_FP16;
+    zero_hparams_t hp{};
+    AdamK k{};
+    // stages 0-2
+    uint64_t shard = 0, padded = 0;
+    // stage 3
+    std::vector<uint64_t> unit_len, unit_slice, unit_off;
+    uint64_t shard_total = 0;
+    // what zero_step runs
+    uint64_t n = 0, rank_stride = 0;
+    int path = PATH_FUSED;
+    const void* fn_a = nullptr;
+    const void* fn_b = nullptr;
+    int grid_a = 1, grid_b = 1;
+    uint64_t workspace = 0;
+    // device
+    int device = 0, sms = 1;
+    DevState* d_state = nullptr;
+    DevScalars* h_mirror = nullptr;     // pinned: DevScalars followed by DevStatus
+    cudaEvent_t ev_done = nullptr;
+    cudaStream_t copy_stream = nullptr;
+    bool stepped = false;
+    // diagnostics
+    bool profile = false;
+    std::vector<ProfileSlot> ring;
+    int ring_pos = 0;
+    double ms_a = 0.0, ms_b = 0.0;
+    int64_t prof_steps = 0;
+    int64_t launches = 0;
+};
+
+namespace {
+
+uint64_t round_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
+uint64_t ceil_div(uint64_t a, uint64_t b) { return (a + b - 1) / b; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool finite_f(float x) { return std::isfinite(x); }
+
+zero_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? ZERO_OK : ZERO_ECUDA; }
+
+zero_status_t check_hparams(const zero_hparams_t& h, zero_dtype_t dtype)
+{
+    if (!finite_f(h.lr) || !finite_f(h.eps) || h.eps < 0.0f) return ZERO_EINVAL;
+    if (!(h.beta1 >= 0.0f && h.beta1 < 1.0f) || !(h.beta2 >= 0.0f && h.beta2 < 1.0f))
+        return ZERO_EINVAL;
+    if (!finite_f(h.weight_decay) || !finite_f(h.clip_norm) || h.clip_norm < 0.0f)
+        return ZERO_EINVAL;
+    if (!finite_f(h.loss_scale) || !(h.loss_scale > 0.0f)) return ZERO_EINVAL;
+    if (h.dynamic_scale) {
+        if (dtype != ZERO_FP16) return ZERO_EINVAL;
+        if (!(h.backoff > 0.0f && h.backoff <= 1.0f)) return ZERO_EINVAL;
+    }
+    return ZERO_OK;
+}
+
+void destroy_plan(zero_plan* p)
+{
+    if (!p) return;
+    for (auto& s : p->ring)
+        for (auto& e : s.ev)
+            if (e) cudaEventDestroy(e);
+    if (p->d_state) cudaFree(p->d_state);
+    if (p->h_mirror) cudaFreeHost(p->h_mirror);
+    if (p->ev_done) cudaEventDestroy(p->ev_done);
+    if (p->copy_stream) cudaStreamDestroy(p->copy_stream);
+    delete p;
+}
+
+// Largest grid the kernel keeps resident on every SM, capped by the work
+// (one thread per 8-element vector) and by the per-block partials array.
+int grid_for(const void* fn, int sms, uint64_t n)
+{
+    int occ = 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, ZERO_THREADS, 0) != cudaSuccess ||
+        occ < 1)
+        occ = 1;
+    const uint64_t want = std::max<uint64_t>(1, ceil_div(n / 8, ZERO_THREADS));
+    uint64_t g = std::min<uint64_t>((uint64_t)sms * (uint64_t)occ, want);
+    g = std::min<uint64_t>(g, ZERO_MAX_BLOCKS);
+    return (int)std::max<uint64_t>(g, 1);
+}
+
+zero_status_t create_impl(uint64_t psi, int nd, int stage, zero_dtype_t dtype,
+                          const int64_t* dims, const int* ndims, int ntensors,
+                          const int* unit_of_tensor, const zero_hparams_t* hp, zero_plan_t* out)
+{
+    if (!out || !hp) return ZERO_EINVAL;
+    *out = nullptr;
+    if (nd < 1 || nd > ZERO_MAX_ND || stage < 0 || stage > 3) return ZERO_EINVAL;
+    if (dtype != ZERO_FP16 && dtype != ZERO_BF16) return ZERO_EINVAL;
+    if (ntensors < 0 || (ntensors > 0 && (!dims || !ndims))) return ZERO_EINVAL;
+    zero_status_t s = check_hparams(*hp, dtype);
+    if (s != ZERO_OK) return s;
+
+    // tensor sizes; their sum must be psi
+    std::vector<uint64_t> tlen((size_t)ntensors);
+    uint64_t total = 0;
+    size_t di = 0;
+    for (int t = 0; t < ntensors; t++) {
+        if (ndims[t] < 0 || ndims[t] > 16) return ZERO_EINVAL;
+        uint64_t len = 1;
+        for (int d = 0; d < ndims[t]; d++) {
+            const int64_t x = dims[di++];
+            if (x < 0) return ZERO_EINVAL;
+            if (x != 0 && len > UINT64_MAX / (uint64_t)x) return ZERO_EINVAL;
+            len *= (uint64_t)x;
+        }
+        tlen[(size_t)t] = len;
+        if (total > UINT64_MAX - len) return ZERO_EINVAL;
+        total += len;
+    }
+    if (total != psi) return ZERO_EINVAL;
+
+    zero_plan* p = new (std::nothrow) zero_plan();
+    if (!p) return ZERO_ENOMEM;
+    p->psi = psi;
+    p->nd = nd;
+    p->stage = stage;
+    p->dtype = dtype;
+    p->hp = *hp;
+
+    if (stage <= 2) {
+        p->shard = round_up(ceil_div(psi, (uint64_t)nd), LAYOUT_ALIGN);
+        p->padded = p->shard * (uint64_t)nd;
+        p->n = psi;
+        p->rank_stride = p->padded;
+    } else {
+        // units: given, or one per tensor; each unit's tensors contiguous
+        int nunits = 0;
+        std::vector<uint64_t> ulen;
+        for (int t = 0; t < ntensors; t++) {
+            const int u = unit_of_tensor ? unit_of_tensor[t] : t;
+            if (u == nunits) {
+                ulen.push_back(0);
+                nunits++;
+            } else if (u != nunits - 1) {
+                destroy_plan(p);
+                return ZERO_EINVAL;
+            }
+            ulen.back() += tlen[(size_t)t];
+        }
+        uint64_t off = 0;
+        for (int u = 0; u < nunits; u++) {
+            const uint64_t sl = round_up(ceil_div(ulen[(size_t)u], (uint64_t)nd), LAYOUT_ALIGN);
+            p->unit_len.push_back(ulen[(size_t)u]);
+            p->unit_slice.push_back(sl);
+            p->unit_off.push_back(off);
+            off += sl;
+        }
+        p->shard_total = off;
+        p->shard = off;
+        p->padded = off;
+        p->n = off;
+        p->rank_stride = off;
+    }
+
+    // Adam constants: 1 - beta1, 1 - beta2 and 1 - lr*wd in double, rounded once
+    p->k.lr = hp->lr;
+    p->k.b1 = hp->beta1;
+    p->k.b2 = hp->beta2;
+    p->k.eps = hp->eps;
+    p->k.wd = hp->weight_decay;
+    p->k.omb1 = (float)(1.0 - (double)hp->beta1);
+    p->k.omb2 = (float)(1.0 - (double)hp->beta2);
+    p->k.decay = (float)(1.0 - (double)hp->lr * (double)hp->weight_decay);
+    p->k.decoupled = hp->decoupled_wd ? 1 : 0;
+    p->k.use_wd = hp->weight_decay != 0.0f;
+
+    // kernel path
+    const bool needs_global = hp->clip_norm > 0.0f || hp->dynamic_scale;
+    int kind_a, kind_b = -1;
+    if (!needs_global) {
+        p->path = PATH_FUSED;
+        kind_a = K_FUSED;
+    } else if (nd >= 4) {
+        p->path = PATH_G32;
+        kind_a = K_REDUCE_G32;
+        kind_b = K_UPDATE_G32;
+        p->workspace = round_up(p->n * sizeof(float), 256);
+    } else {
+        p->path = PATH_RECOMPUTE;
+        kind_a = K_REDUCE_ONLY;
+        kind_b = K_UPDATE_RECOMPUTE;
+    }
+    p->fn_a = step_kernel((int)dtype, kind_a, nd);
+    p->fn_b = kind_b >= 0 ? step_kernel((int)dtype, kind_b, nd) : nullptr;
+    if (!p->fn_a || (kind_b >= 0 && !p->fn_b)) {
+        destroy_plan(p);
+        return ZERO_EINVAL;
+    }
+
+    // device resources
+    cudaError_t e = cudaGetDevice(&p->device);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&p->sms, cudaDevAttrMultiProcessorCount, p->device);
+    if (e != cudaSuccess) {
+        destroy_plan(p);
+        return ZERO_ECUDA;
+    }
+    p->grid_a = grid_for(p->fn_a, p->sms, p->n);
+    p->grid_b = p->fn_b ? grid_for(p->fn_b, p->sms, p->n) : 1;
+
+    if (cudaMalloc(&p->d_state, sizeof(DevState)) != cudaSuccess ||
+        cudaMallocHost(&p->h_mirror, sizeof(DevScalars) + sizeof(DevStatus)) != cudaSuccess) {
+        destroy_plan(p);
+        return ZERO_ENOMEM;
+    }
+    DevState* init = new (std::nothrow) DevState();
+    if (!init) {
+        destroy_plan(p);
+        return ZERO_ENOMEM;
+    }
+    std::memset(init, 0, sizeof(DevState));
+    init->sc.loss_scale = hp->loss_scale;
+    init->sc.good_steps = 0;
+    init->sc.t = 0;
+    init->sc.beta1_pow = 1.0;
+    init->sc.beta2_pow = 1.0;
+    init->st.clip_coef = 1.0f;
+    init->st.used_scale = hp->loss_scale;
+    e = cudaMemcpy(p->d_state, init, sizeof(DevState), cudaMemcpyHostToDevice);
+    std::memcpy(p->h_mirror, &init->sc, sizeof(DevScalars));
+    std::memcpy(reinterpret_cast<char*>(p->h_mirror) + sizeof(DevScalars), &init->st,
+                sizeof(DevStatus));
+    delete init;
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_done, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->copy_stream, cudaStreamNonBlocking);
+    if (e != cudaSuccess) {
+        destroy_plan(p);
+        return ZERO_ECUDA;
+    }
+    *out = p;
+    return ZERO_OK;
+}
+
+void harvest(zero_plan* p, ProfileSlot& s)
+{
+    if (!s.used) return;
+    float a = 0.0f, b = 0.0f;
+    if (cudaEventSynchronize(s.ev[2]) == cudaSuccess &&
+        cudaEventElapsedTime(&a, s.ev[0], s.ev[1]) == cudaSuccess &&
+        cudaEventElapsedTime(&b, s.ev[1], s.ev[2]) == cudaSuccess) {
+        p->ms_a += a;
+        p->ms_b += b;
+        p->prof_steps += 1;
+    }
+    s.used = false;
+}
+
+zero_status_t fetch_mirror(zero_plan* p)
+{
+    if (!p->stepped) return ZERO_OK;
+    cudaError_t e = cudaEventSynchronize(p->ev_done);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(p->h_mirror, p->d_state, sizeof(DevScalars) + sizeof(DevStatus),
+                            cudaMemcpyDeviceToHost, p->copy_stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(p->copy_stream);
+    return cuda_status(e);
+}
+
+}  // namespace
+
+namespace zero {
+const void* step_kernel(int dtype, int kind, int nd)
+{
+    return dtype == 0 ? step_kernel_fp16(kind, nd) : step_kernel_bf16(kind, nd);
+}
+}  // namespace zero
+
+extern "C" {
+
+zero_status_t zero_plan_create(uint64_t psi, int nd, int stage, zero_dtype_t dtype,
+                               const int64_t* dims, const int* ndims, int ntensors,
+                               const zero_hparams_t* hp, zero_plan_t* out)
+{
+    return create_impl(psi, nd, stage, dtype, dims, ndims, ntensors, nullptr, hp, out);
+}
+
+zero_status_t zero_plan_create_units(uint64_t psi, int nd, int stage, zero_dtype_t dtype,
+                                     const int64_t* dims, const int* ndims, int ntensors,
+                                     const int* unit_of_tensor, const zero_hparams_t* hp,
+                                     zero_plan_t* out)
+{
+    if (stage == 3 && ntensors > 0 && !unit_of_tensor) return ZERO_EINVAL;
+    return create_impl(psi, nd, stage, dtype, dims, ndims, ntensors, unit_of_tensor, hp, out);
+}
+
+zero_status_t zero_plan_destroy(zero_plan_t plan)
+{
+    if (plan && plan->stepped) cudaEventSynchronize(plan->ev_done);
+    destroy_plan(plan);
+    return ZERO_OK;
+}
+
+zero_status_t zero_plan_layout(zero_plan_t plan, uint64_t* shard_elems, uint64_t* padded_elems,
+                               int* nunits, uint64_t* workspace_bytes)
+{
+    if (!plan) return ZERO_EINVAL;
+    if (shard_elems) *shard_elems = plan->shard;
+    if (padded_elems) *padded_elems = plan->padded;
+    if (nunits) *nunits = plan->stage == 3 ? (int)plan->unit_len.size() : 0;
+    if (workspace_bytes) *workspace_bytes = plan->workspace;
+    return ZERO_OK;
+}
+
+zero_status_t zero_plan_unit(zero_plan_t plan, int unit, uint64_t* len, uint64_t* slice_elems,
+                             uint64_t* offset)
+{
+    if (!plan || plan->stage != 3 || unit < 0 || unit >= (int)plan->unit_len.size())
+        return ZERO_EINVAL;
+    if (len) *len = plan->unit_len[(size_t)unit];
+    if (slice_elems) *slice_elems = plan->unit_slice[(size_t)unit];
+    if (offset) *offset = plan->unit_off[(size_t)unit];
+    return ZERO_OK;
+}
+
+int zero_plan_path(zero_plan_t plan) { return plan ? plan->path : -1; }
+
+zero_status_t zero_step(zero_plan_t plan, const void* grads, float* master, float* m, float* v,
+                        void* params, void* workspace, void* stream)
+{
+    if (!plan) return ZERO_EINVAL;
+    if (plan->n > 0) {
+        const void* ptrs[] = {grads, master, m, v, params};
+        for (const void* q : ptrs)
+            if (!q || !aligned16(q)) return ZERO_EINVAL;
+    }
+    if (plan->path == PATH_G32 && plan->n > 0 && (!workspace || !aligned16(workspace)))
+        return ZERO_EINVAL;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ZERO_ECUDA;
+    if (dev != plan->device) return ZERO_EINVAL;
+
+    StepArgs a;
+    a.grads = static_cast<const uint16_t*>(grads);
+    a.master = master;
+    a.m = m;
+    a.v = v;
+    a.params = static_cast<uint16_t*>(params);
+    a.g32 = static_cast<float*>(workspace);
+    a.n = (int64_t)plan->n;
+    a.rank_stride = (int64_t)plan->rank_stride;
+    a.nd = plan->nd;
+    a.k = plan->k;
+    a.clip = plan->hp.clip_norm;
+    a.dynamic = plan->hp.dynamic_scale ? 1 : 0;
+    a.backoff = plan->hp.backoff;
+    a.growth_interval = plan->hp.growth_interval;
+    a.state = plan->d_state;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    ProfileSlot* slot = nullptr;
+    if (plan->profile) {
+        slot = &plan->ring[(size_t)(plan->ring_pos % PROFILE_RING)];
+        harvest(plan, *slot);
+        plan->ring_pos++;
+        if (cudaEventRecord(slot->ev[0], s) != cudaSuccess) return ZERO_ECUDA;
+    }
+    void* args[] = {&a};
+    cudaError_t e = cudaLaunchKernel(plan->fn_a, dim3(plan->grid_a), dim3(ZERO_THREADS), args, 0, s);
+    if (e != cudaSuccess) return ZERO_ECUDA;
+    plan->launches++;
+    if (slot && cudaEventRecord(slot->ev[1], s) != cudaSuccess) return ZERO_ECUDA;
+    if (plan->fn_b) {
+        e = cudaLaunchKernel(plan->fn_b, dim3(plan->grid_b), dim3(ZERO_THREADS), args, 0, s);
+        if (e != cudaSuccess) return ZERO_ECUDA;
+        plan->launches++;
+    }
+    if (slot) {
+        if (cudaEventRecord(slot->ev[2], s) != cudaSuccess) return ZERO_ECUDA;
+        slot->used = true;
+    }
+    if (cudaEventRecord(plan->ev_done, s) != cudaSuccess) return ZERO_ECUDA;
+    plan->stepped = true;
+    return ZERO_OK;
+}
+
+zero_status_t zero_step_result(zero_plan_t plan, int* skipped, double* grad_norm,
+                               float* clip_coef, float* loss_scale, int64_t* t)
+{
+    if (!plan) return ZERO_EINVAL;
+    zero_status_t s = fetch_mirror(plan);
+    if (s != ZERO_OK) return s;
+    const DevScalars* sc = plan->h_mirror;
+    const DevStatus* st = reinterpret_cast<const DevStatus*>(
+        reinterpret_cast<const char*>(plan->h_mirror) + sizeof(DevScalars));
+    if (skipped) *skipped = st->skipped;
+    if (grad_norm) *grad_norm = st->grad_norm;
+    if (clip_coef) *clip_coef = st->clip_coef;
+    if (loss_scale) *loss_scale = sc->loss_scale;
+    if (t) *t = sc->t;
+    return ZERO_OK;
+}
+
+zero_status_t zero_step_overflow(zero_plan_t plan, int* overflow)
+{
+    if (!plan || !overflow) return ZERO_EINVAL;
+    zero_status_t s = fetch_mirror(plan);
+    if (s != ZERO_OK) return s;
+    const DevStatus* st = reinterpret_cast<const DevStatus*>(
+        reinterpret_cast<const char*>(plan->h_mirror) + sizeof(DevScalars));
+    *overflow = st->overflow;
+    return ZERO_OK;
+}
+
+zero_status_t zero_gather_layer(zero_plan_t plan, int unit, const void* const* shard_ptrs,
+                                void* out, void* stream)
+{
+    if (!plan || plan->stage != 3 || unit < 0 || unit >= (int)plan->unit_len.size())
+        return ZERO_EINVAL;
+    if (!shard_ptrs || !out || !aligned16(out)) return ZERO_EINVAL;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ZERO_ECUDA;
+    if (dev != plan->device) return ZERO_EINVAL;
+    GatherArgs* a = new (std::nothrow) GatherArgs();
+    if (!a) return ZERO_ENOMEM;
+    const uint64_t off = plan->unit_off[(size_t)unit];
+    for (int k = 0; k < plan->nd; k++) {
+        const uint16_t* b = static_cast<const uint16_t*>(shard_ptrs[k]);
+        if (!b || !aligned16(b)) {
+            delete a;
+            return ZERO_EINVAL;
+        }
+        a->src[k] = b + off;
+    }
+    a->out = static_cast<uint16_t*>(out);
+    a->len = (int64_t)plan->unit_len[(size_t)unit];
+    a->slice = (int64_t)plan->unit_slice[(size_t)unit];
+    a->nd = plan->nd;
+    cudaError_t e = cudaSuccess;
+    if (a->len > 0) {
+        e = launch_gather(*a, plan->sms, static_cast<cudaStream_t>(stream));
+        if (e == cudaSuccess) plan->launches++;
+    }
+    delete a;
+    return cuda_status(e);
+}
+
+uint64_t zero_state_bytes(uint64_t psi, uint64_t nd, int stage, int K)
+{
+    if (nd == 0 || K < 0) return 0;
+    using u128 = unsigned __int128;
+    const u128 P = psi, N = nd, k = (u128)K;
+    u128 r;
+    switch (stage) {
+    case 0: r = (4 + k) * P; break;
+    case 1: r = 4 * P + (k * P + N - 1) / N; break;
+    case 2: r = 2 * P + ((2 + k) * P + N - 1) / N; break;
+    case 3: r = ((4 + k) * P + N - 1) / N; break;
+    default: return 0;
+    }
+    return r > (u128)UINT64_MAX ? UINT64_MAX : (uint64_t)r;
+}
+
+uint64_t zero_comm_volume(uint64_t psi, uint64_t nd, int stage, int exact)
+{
+    if (nd == 0 || stage < 0 || stage > 3) return 0;
+    using u128 = unsigned __int128;
+    const u128 v = (u128)(stage == 3 ? 3 : 2) * psi;
+    const u128 r = exact ? (v * (nd - 1) + nd - 1) / nd : v;
+    return r > (u128)UINT64_MAX ? UINT64_MAX : (uint64_t)r;
+}
+
+uint64_t zero_max_params(uint64_t mem_bytes, uint64_t nd, int stage, int K)
+{
+    if (nd == 0 || K < 0) return 0;
+    using u128 = unsigned __int128;
+    const u128 M = mem_bytes, N = nd, k = (u128)K;
+    u128 r;
+    switch (stage) {
+    case 0: r = M / (4 + k); break;
+    case 1: r = M * N / (4 * N + k); break;
+    case 2: r = M * N / (2 * N + 2 + k); break;
+    case 3: r = M * N / (4 + k); break;
+    default: return 0;
+    }
+    return r > (u128)UINT64_MAX ? UINT64_MAX : (uint64_t)r;
+}
+
+const char* zero_status_string(zero_status_t status)
+{
+    switch (status) {
+    case ZERO_OK: return "ZERO_OK";
+    case ZERO_EINVAL: return "ZERO_EINVAL: invalid argument";
+    case ZERO_ENOMEM: return "ZERO_ENOMEM: allocation failed";
+    case ZERO_ECUDA: return "ZERO_ECUDA: CUDA call failed";
+    case ZERO_ETIMEOUT: return "ZERO_ETIMEOUT: bounded device wait gave up";
+    default: return "unknown zero_status_t";
+    }
+}
+
+zero_status_t zero_plan_profile(zero_plan_t plan, int enable)
+{
+    if (!plan) return ZERO_EINVAL;
+    if (!enable) {
+        plan->profile = false;
+        return ZERO_OK;
+    }
+    if (plan->ring.empty()) {
+        plan->ring.resize(PROFILE_RING);
+        for (auto& s : plan->ring)
+            for (auto& e : s.ev)
+                if (cudaEventCreate(&e) != cudaSuccess) return ZERO_ECUDA;
+    }
+    for (auto& s : plan->ring) {
+        if (s.used) cudaEventSynchronize(s.ev[2]);
+        s.used = false;
+    }
+    plan->ms_a = plan->ms_b = 0.0;
+    plan->prof_steps = 0;
+    plan->ring_pos = 0;
+    plan->profile = true;
+    return ZERO_OK;
+}
+
+zero_status_t zero_plan_kernel_times(zero_plan_t plan, double* reduce_ms, double* update_ms,
+                                     int64_t* steps, int64_t* launches)
+{
+    if (!plan) return ZERO_EINVAL;
+    if (!plan->ring.empty()) {
+        const int start = plan->ring_pos;
+        for (int i = 0; i < PROFILE_RING; i++)
+            harvest(plan, plan->ring[(size_t)((start + i) % PROFILE_RING)]);
+    }
+    if (reduce_ms) *reduce_ms = plan->ms_a;
+    if (update_ms) *update_ms = plan->ms_b;
+    if (steps) *steps = plan->prof_steps;
+    if (launches) *launches = plan->launches;
+    return ZERO_OK;
+}
+
+}  // extern "C"

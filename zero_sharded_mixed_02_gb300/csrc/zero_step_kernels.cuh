@@ -1,0 +1,277 @@
+// zero_step_kernels.cuh -- the optimizer-step kernels (templates).
+//
+// Grid: a persistent grid of ZERO_THREADS-thread blocks, sized once per plan
+// from the SM count and the kernel's occupancy.  Thread t of block b handles
+// the 8-element vectors b*T + t, b*T + t + G*T, ... (static assignment), so the
+// per-block sums of squares and their fixed-order combination are the same on
+// every run.  The last block to finish (an atomic ticket, no waiting) combines
+// the per-block partials in block order and writes the step status.
+#pragma once
+
+#include "zero_common.cuh"
+
+namespace zero {
+
+// Norm partial of one group of 8: an FMA chain in binary32, moved to binary64
+// per group.  Groups whose binary32 sum of squares would lose range (very large
+// or very small gradients) are summed exactly in binary64 instead.
+static __device__ __forceinline__ double group_sumsq(const float (&g)[8])
+{
+    float q = 0.0f;
+    int nz = 0;
+#pragma unroll
+    for (int e = 0; e < 8; e++) {
+        q = __fmaf_rn(g[e], g[e], q);
+        nz |= (g[e] != 0.0f);
+    }
+    if ((q > 1.2676506e30f || q < 8.6736174e-19f) && nz) {   // 2^100, 2^-60
+        double d = 0.0;
+#pragma unroll
+        for (int e = 0; e < 8; e++) d = __fma_rn((double)g[e], (double)g[e], d);
+        return d;
+    }
+    return (double)q;
+}
+
+// Scalar bookkeeping of the step (thread 0 of the last block): global norm,
+// clip coefficient, skip decision, loss-scale backoff/growth, t and the bias
+// corrections.  Binary64 operations are IEEE round-to-nearest.
+static __device__ __noinline__ void finalize(const StepArgs a, double sumsq, int overflow)
+{
+    DevState* S = a.state;
+    DevScalars sc = S->sc;
+    DevStatus st;
+    st.overflow   = overflow;
+    st.used_scale = sc.loss_scale;
+    st.grad_norm  = __dsqrt_rn(sumsq);
+    st.clip_coef  = (a.clip > 0.0f && st.grad_norm > (double)a.clip)
+                        ? __double2float_rn(__ddiv_rn((double)a.clip, st.grad_norm)) : 1.0f;
+    st.err = 0;
+    st.pad = 0;
+    if (overflow && a.dynamic) {
+        st.skipped = 1;
+        sc.loss_scale = __fmul_rn(sc.loss_scale, a.backoff);
+        sc.good_steps = 0;
+        st.bc1 = st.bc2 = 0.0f;
+    } else {
+        st.skipped = 0;
+        sc.t += 1;
+        sc.beta1_pow = __dmul_rn(sc.beta1_pow, (double)a.k.b1);
+        sc.beta2_pow = __dmul_rn(sc.beta2_pow, (double)a.k.b2);
+        st.bc1 = __double2float_rn(__dsub_rn(1.0, sc.beta1_pow));
+        st.bc2 = __double2float_rn(__dsub_rn(1.0, sc.beta2_pow));
+        if (a.dynamic && a.growth_interval > 0) {
+            sc.good_steps += 1;
+            if (sc.good_steps >= a.growth_interval) {
+                sc.loss_scale = __fmul_rn(sc.loss_scale, 2.0f);
+                sc.good_steps = 0;
+            }
+        }
+    }
+    S->sc = sc;
+    S->st = st;
+}
+
+struct RedShared {
+    double d[ZERO_THREADS / 32];
+    int    i[ZERO_THREADS / 32];
+    int    last;
+};
+
+// Publish this block's partial; the last block to arrive finalizes the step.
+static __device__ __forceinline__ void reduce_and_finalize(const StepArgs& a, double acc, int bad,
+                                                    RedShared& sh)
+{
+    const double bsum = block_sum(acc, sh.d);
+    const int    bbad = block_or(bad, sh.i);
+    if (threadIdx.x == 0) {
+        a.state->partial[blockIdx.x] = bsum;
+        a.state->flag[blockIdx.x]    = bbad;
+        __threadfence();
+        const unsigned ticket = atomicAdd(&a.state->counter, 1u);
+        sh.last = (ticket == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (!sh.last) return;
+    __threadfence();
+    double x = 0.0;
+    int f = 0;
+    for (int b = threadIdx.x; b < (int)gridDim.x; b += blockDim.x) {
+        x += __ldcg(&a.state->partial[b]);
+        f |= __ldcg(&a.state->flag[b]);
+    }
+    const double total = block_sum(x, sh.d);
+    const int    any   = block_or(f, sh.i);
+    if (threadIdx.x == 0) {
+        finalize(a, total, any);
+        a.state->counter = 0;
+    }
+}
+
+static __device__ __forceinline__ void unpack8(const float4 a, const float4 b, float (&x)[8])
+{
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
+// ---- pass 1: stages 1-3a (fold, average, unscale, flag, squares) ----------
+template <int DT, int ND, bool WRITE_G>
+__global__ void __launch_bounds__(ZERO_THREADS) k_reduce(const StepArgs a)
+{
+    __shared__ RedShared sh;
+    const int nd = ND > 0 ? ND : a.nd;
+    Unscale un;
+    un.init(nd, a.state->sc.loss_scale);
+    double acc = 0.0;
+    int bad = 0;
+    const int64_t nvec = a.n >> 3;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t vi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; vi < nvec; vi += stride) {
+        float s[8], g[8];
+        fold8<DT, ND>(a.grads, a.rank_stride, vi, nd, s);
+#pragma unroll
+        for (int e = 0; e < 8; e++) {
+            g[e] = un(s[e]);
+            bad |= not_finite(g[e]);
+        }
+        acc += group_sumsq(g);
+        if (WRITE_G) {
+            float4* o = reinterpret_cast<float4*>(a.g32) + 2 * vi;
+            __stcs(o, make_float4(g[0], g[1], g[2], g[3]));
+            __stcs(o + 1, make_float4(g[4], g[5], g[6], g[7]));
+        }
+    }
+    if (blockIdx.x == 0 && threadIdx.x < 8) {            // the ragged tail (< 8 elements)
+        const int64_t i = (nvec << 3) + threadIdx.x;
+        if (i < a.n) {
+            const float g = un(fold1<DT>(a.grads, a.rank_stride, i, nd));
+            bad |= not_finite(g);
+            acc = __fma_rn((double)g, (double)g, acc);
+            if (WRITE_G) a.g32[i] = g;
+        }
+    }
+    reduce_and_finalize(a, acc, bad, sh);
+}
+
+// ---- pass 2: stages 4-6a (clip, Adam, cast, write-back) -------------------
+template <int DT, int ND, bool RECOMPUTE>
+__global__ void __launch_bounds__(ZERO_THREADS) k_update(const StepArgs a)
+{
+    const DevStatus st = a.state->st;
+    if (st.skipped) return;
+    const int nd = ND > 0 ? ND : a.nd;
+    Unscale un;
+    un.init(nd, st.used_scale);
+    const float c = st.clip_coef, bc1 = st.bc1, bc2 = st.bc2;
+    const int64_t nvec = a.n >> 3;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    float4* pm = reinterpret_cast<float4*>(a.master);
+    float4* mm = reinterpret_cast<float4*>(a.m);
+    float4* vv = reinterpret_cast<float4*>(a.v);
+    for (int64_t vi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; vi < nvec; vi += stride) {
+        float g[8], p[8], m[8], v[8];
+        const float4 p0 = __ldcs(pm + 2 * vi), p1 = __ldcs(pm + 2 * vi + 1);
+        const float4 m0 = __ldcs(mm + 2 * vi), m1 = __ldcs(mm + 2 * vi + 1);
+        const float4 v0 = __ldcs(vv + 2 * vi), v1 = __ldcs(vv + 2 * vi + 1);
+        if (RECOMPUTE) {
+            float s[8];
+            fold8<DT, ND>(a.grads, a.rank_stride, vi, nd, s);
+#pragma unroll
+            for (int e = 0; e < 8; e++) g[e] = un(s[e]);
+        } else {
+            const float4* gv = reinterpret_cast<const float4*>(a.g32) + 2 * vi;
+            unpack8(__ldcs(gv), __ldcs(gv + 1), g);
+        }
+        unpack8(p0, p1, p);
+        unpack8(m0, m1, m);
+        unpack8(v0, v1, v);
+#pragma unroll
+        for (int e = 0; e < 8; e++) adam1(g[e], c, p[e], m[e], v[e], bc1, bc2, a.k);
+        __stcs(pm + 2 * vi, make_float4(p[0], p[1], p[2], p[3]));
+        __stcs(pm + 2 * vi + 1, make_float4(p[4], p[5], p[6], p[7]));
+        __stcs(mm + 2 * vi, make_float4(m[0], m[1], m[2], m[3]));
+        __stcs(mm + 2 * vi + 1, make_float4(m[4], m[5], m[6], m[7]));
+        __stcs(vv + 2 * vi, make_float4(v[0], v[1], v[2], v[3]));
+        __stcs(vv + 2 * vi + 1, make_float4(v[4], v[5], v[6], v[7]));
+        __stcs(reinterpret_cast<uint4*>(a.params) + vi,
+               make_uint4(narrow2<DT>(p[0], p[1]), narrow2<DT>(p[2], p[3]),
+                          narrow2<DT>(p[4], p[5]), narrow2<DT>(p[6], p[7])));
+    }
+    if (blockIdx.x == 0 && threadIdx.x < 8) {
+        const int64_t i = (nvec << 3) + threadIdx.x;
+        if (i < a.n) {
+            const float g = RECOMPUTE ? un(fold1<DT>(a.grads, a.rank_stride, i, nd)) : a.g32[i];
+            float p = a.master[i], m = a.m[i], v = a.v[i];
+            adam1(g, c, p, m, v, bc1, bc2, a.k);
+            a.master[i] = p;
+            a.m[i] = m;
+            a.v[i] = v;
+            a.params[i] = narrow1<DT>(p);
+        }
+    }
+}
+
+// ---- fused single pass (no clip, no dynamic scale): stages 1-6a ------------
+template <int DT, int ND>
+__global__ void __launch_bounds__(ZERO_THREADS) k_fused(const StepArgs a)
+{
+    __shared__ RedShared sh;
+    const DevScalars sc = a.state->sc;
+    const int nd = ND > 0 ? ND : a.nd;
+    Unscale un;
+    un.init(nd, sc.loss_scale);
+    // bias corrections of step t+1 (this path never skips)
+    const float bc1 = __double2float_rn(__dsub_rn(1.0, __dmul_rn(sc.beta1_pow, (double)a.k.b1)));
+    const float bc2 = __double2float_rn(__dsub_rn(1.0, __dmul_rn(sc.beta2_pow, (double)a.k.b2)));
+    double acc = 0.0;
+    int bad = 0;
+    const int64_t nvec = a.n >> 3;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    float4* pm = reinterpret_cast<float4*>(a.master);
+    float4* mm = reinterpret_cast<float4*>(a.m);
+    float4* vv = reinterpret_cast<float4*>(a.v);
+    for (int64_t vi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; vi < nvec; vi += stride) {
+        float s[8], g[8], p[8], m[8], v[8];
+        const float4 p0 = __ldcs(pm + 2 * vi), p1 = __ldcs(pm + 2 * vi + 1);
+        const float4 m0 = __ldcs(mm + 2 * vi), m1 = __ldcs(mm + 2 * vi + 1);
+        const float4 v0 = __ldcs(vv + 2 * vi), v1 = __ldcs(vv + 2 * vi + 1);
+        fold8<DT, ND>(a.grads, a.rank_stride, vi, nd, s);
+#pragma unroll
+        for (int e = 0; e < 8; e++) {
+            g[e] = un(s[e]);
+            bad |= not_finite(g[e]);
+        }
+        acc += group_sumsq(g);
+        unpack8(p0, p1, p);
+        unpack8(m0, m1, m);
+        unpack8(v0, v1, v);
+#pragma unroll
+        for (int e = 0; e < 8; e++) adam1(g[e], 1.0f, p[e], m[e], v[e], bc1, bc2, a.k);
+        __stcs(pm + 2 * vi, make_float4(p[0], p[1], p[2], p[3]));
+        __stcs(pm + 2 * vi + 1, make_float4(p[4], p[5], p[6], p[7]));
+        __stcs(mm + 2 * vi, make_float4(m[0], m[1], m[2], m[3]));
+        __stcs(mm + 2 * vi + 1, make_float4(m[4], m[5], m[6], m[7]));
+        __stcs(vv + 2 * vi, make_float4(v[0], v[1], v[2], v[3]));
+        __stcs(vv + 2 * vi + 1, make_float4(v[4], v[5], v[6], v[7]));
+        __stcs(reinterpret_cast<uint4*>(a.params) + vi,
+               make_uint4(narrow2<DT>(p[0], p[1]), narrow2<DT>(p[2], p[3]),
+                          narrow2<DT>(p[4], p[5]), narrow2<DT>(p[6], p[7])));
+    }
+    if (blockIdx.x == 0 && threadIdx.x < 8) {
+        const int64_t i = (nvec << 3) + threadIdx.x;
+        if (i < a.n) {
+            const float g = un(fold1<DT>(a.grads, a.rank_stride, i, nd));
+            bad |= not_finite(g);
+            acc = __fma_rn((double)g, (double)g, acc);
+            float p = a.master[i], m = a.m[i], v = a.v[i];
+            adam1(g, 1.0f, p, m, v, bc1, bc2, a.k);
+            a.master[i] = p;
+            a.m[i] = m;
+            a.v[i] = v;
+            a.params[i] = narrow1<DT>(p);
+        }
+    }
+    reduce_and_finalize(a, acc, bad, sh);
+}
+
+}  // namespace zero

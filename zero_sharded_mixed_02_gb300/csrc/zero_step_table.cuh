@@ -1,0 +1,46 @@
+// zero_step_table.cuh -- the template instances one 16-bit format needs.
+// Rank counts with a compiled-in loop (1, 2, 4, 8, 16, 32, 64) get a fully
+// unrolled fold; any other count uses the generic instance (ND = 0).
+#pragma once
+
+#include "zero_launch.h"
+#include "zero_step_kernels.cuh"
+
+namespace zero {
+
+template <int DT, int ND>
+static const void* fused_or_reduce(int kind)
+{
+    switch (kind) {
+    case K_FUSED: return (const void*)k_fused<DT, ND>;
+    case K_REDUCE_G32:
+        if constexpr (ND == 0 || ND >= 4) return (const void*)k_reduce<DT, ND, true>;
+        return nullptr;
+    case K_REDUCE_ONLY:
+        if constexpr (ND == 0 || ND < 4) return (const void*)k_reduce<DT, ND, false>;
+        return nullptr;
+    case K_UPDATE_RECOMPUTE:
+        if constexpr (ND == 0 || ND < 4) return (const void*)k_update<DT, ND, true>;
+        return nullptr;
+    case K_UPDATE_G32:
+        return (const void*)k_update<DT, 0, false>;
+    default: return nullptr;
+    }
+}
+
+template <int DT>
+static const void* step_kernel_dt(int kind, int nd)
+{
+    switch (nd) {
+    case 1:  return fused_or_reduce<DT, 1>(kind);
+    case 2:  return fused_or_reduce<DT, 2>(kind);
+    case 4:  return fused_or_reduce<DT, 4>(kind);
+    case 8:  return fused_or_reduce<DT, 8>(kind);
+    case 16: return fused_or_reduce<DT, 16>(kind);
+    case 32: return fused_or_reduce<DT, 32>(kind);
+    case 64: return fused_or_reduce<DT, 64>(kind);
+    default: return fused_or_reduce<DT, 0>(kind);
+    }
+}
+
+}  // namespace zero
