@@ -167,14 +167,22 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------- workload
-def workload():
+def workload(psi=None):
+    """The GPT-2 1.5B workload; with psi, a flat single-tensor model of psi
+    parameters under the same settings (small cases for profiling)."""
+    import dataclasses
     from gen import workloads
-    return workloads.gpt2_xl()
+    w = workloads.gpt2_xl()
+    if psi:
+        w = dataclasses.replace(w, name=f"flat-{psi}", shapes=[(psi,)])
+    return w
 
 
 def config_of(w, padded):
-    return {"workload": f"{w.name}: GPT-2 1.5B parameter list (48 layers, h=1600, ffn=6400, "
-                        f"vocab 50257, ctx 1024), {len(w.shapes)} tensors",
+    desc = (f"{w.name}: GPT-2 1.5B parameter list (48 layers, h=1600, ffn=6400, vocab 50257, "
+            f"ctx 1024), {len(w.shapes)} tensors" if len(w.shapes) > 1 else
+            f"{w.name}: one flat tensor of {w.psi} parameters, GPT-2 1.5B settings")
+    return {"workload": desc,
             "psi": w.psi, "nd": w.nd, "zero_stage": w.stage, "padded_elems": padded,
             "grads": "fp16 N(0,1e-3) x 65536 loss scale (dynamic)", "clip_norm": w.clip,
             "optimizer": "Adam lr 1e-3 betas (0.9, 0.999) eps 1e-8",
@@ -228,7 +236,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     zbuild.build()
-    w = workload()
+    w = workload(args.psi)
     hp = z.hparams(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
                    decoupled_wd=w.decoupled_wd, clip_norm=w.clip, loss_scale=w.loss_scale,
                    dynamic_scale=w.dynamic_scale, backoff=0.5, growth_interval=1000)
@@ -386,7 +394,7 @@ def run_reference(args):
     rank, _, ws = dist_env()
     if rank != 0:
         return
-    w = workload()
+    w = workload(args.psi)
     thr = oracle_threads(w.nd)
     n_s = args.ref_sample
     import oracle
@@ -418,6 +426,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=1 << 23)
     ap.add_argument("--ref-sample", type=int, default=1 << 21)
+    ap.add_argument("--psi", type=int, default=0,
+                    help="flat model of this many parameters (profiling small cases)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)          # at least 3 untimed warm-up steps
     if args.impl == "reference":
