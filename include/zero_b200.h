@@ -185,6 +185,35 @@ zero_status_t zero_step_overflow(zero_plan_t plan, int* overflow);
 zero_status_t zero_gather_layer(zero_plan_t plan, int unit, const void* const* shard_ptrs,
                                 void* out, void* stream);
 
+/* ---- gradient norm without allocating ------------------------------------ */
+
+/* No counterpart on the pages: a convenience for callers that may not
+ * allocate device memory (code running under another framework's memory pool
+ * or allocator hooks, or code that only holds pre-allocated buffers and so
+ * cannot create a plan, whose creation allocates).
+ * Computes what zero_step's reduce pass reports: the global L2 norm of the
+ * averaged, unscaled gradient g_i = (sum_r grads[r][i] / nd) / loss_scale (the
+ * sum in rank order, fp32) and whether any g_i is inf/NaN.
+ *   grads        [nd][rank_stride] 16-bit device array, 16-byte aligned; the
+ *                first n elements of each rank's row are used.
+ *   rank_stride  >= n, a multiple of 8.
+ *   norm_out     device pointer to one double (8-byte aligned): the norm.
+ *   overflow_out device pointer to one int: 1 if any g_i is inf/NaN, else 0.
+ * Asynchronous on `stream`.  Allocates nothing: its scratch (one partial per
+ * 2^17-element tile plus a counter, 196,864 bytes) is a fixed device array in
+ * the library that every GPU loading the library keeps until process exit;
+ * hence n is limited to 2^31 elements (ZERO_EINVAL beyond).  The first call on
+ * a device looks up that array's device address (cudaGetSymbolAddress); make
+ * the first call on each device before any stream capture.  Every call shares
+ * the array, so calls whose executions overlap on the GPU (e.g. on two
+ * concurrent streams) race and give wrong results; order them.  The norm
+ * agrees with zero_step's within 1e-5 relative (the partial sums are grouped
+ * differently); the flag is identical.
+ * Errors: ZERO_EINVAL (sizes, alignment, null output), ZERO_ECUDA. */
+zero_status_t zero_grad_norm_noalloc(const void* grads, int nd, uint64_t n, uint64_t rank_stride,
+                                     zero_dtype_t dtype, float loss_scale, double* norm_out,
+                                     int* overflow_out, void* stream);
+
 /* ---- memory ledger and communication volume ------------------------------- */
 
 /* Bytes of model state one rank holds ([L18] 1.2, 2.1; [Z026] 2; [L32] 2.1,

@@ -32,6 +32,7 @@ ENTRY_POINTS = (
     "zero_plan_unit", "zero_step", "zero_step_result", "zero_step_overflow",
     "zero_gather_layer", "zero_state_bytes", "zero_comm_volume", "zero_max_params",
     "zero_status_string", "zero_plan_profile", "zero_plan_kernel_times", "zero_plan_path",
+    "zero_grad_norm_noalloc",
 )
 
 
@@ -95,6 +96,8 @@ def lib():
                 "zero_plan_kernel_times": (st, [_P, ctypes.POINTER(ctypes.c_double),
                                                 ctypes.POINTER(ctypes.c_double), _PI64, _PI64]),
                 "zero_plan_path": (ctypes.c_int, [_P]),
+                "zero_grad_norm_noalloc": (st, [_P, ctypes.c_int, _U64, _U64, ctypes.c_int,
+                                                ctypes.c_float, _P, _P, _P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -224,6 +227,17 @@ def zero_plan_kernel_times(plan: int) -> dict:
     _check(lib().zero_plan_kernel_times(plan, ctypes.byref(a), ctypes.byref(b), ctypes.byref(s),
                                         ctypes.byref(n)), "zero_plan_kernel_times")
     return {"reduce_ms": a.value, "update_ms": b.value, "steps": s.value, "launches": n.value}
+
+
+def zero_grad_norm_noalloc(grads, nd: int, n: int, rank_stride: int, dtype: int,
+                           loss_scale: float, norm_out, overflow_out, stream=0) -> None:
+    """Global gradient norm and overflow flag without any allocation: for callers
+    that may not allocate device memory.  norm_out (one float64) and overflow_out
+    (one int32) are device buffers the caller owns; results land there
+    asynchronously on ``stream``."""
+    _check(lib().zero_grad_norm_noalloc(_ptr(grads), nd, n, rank_stride, dtype, loss_scale,
+                                        _ptr(norm_out), _ptr(overflow_out), _ptr(stream)),
+           "zero_grad_norm_noalloc")
 
 
 def psi_of(shapes: Sequence[Sequence[int]]) -> int:
