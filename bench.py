@@ -87,6 +87,39 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+KERNEL_SOURCES = ("zero_common.cuh", "zero_step_kernels.cuh", "zero_step_table.cuh",
+                  "zero_step_fp16.cu", "zero_step_bf16.cu")
+
+
+def kernel_source_sha() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(f.encode())
+        with open(os.path.join(ROOT, "zero_sharded_mixed_02_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def ncu_traffic(kernel: str, psi: int, nd: int):
+    """DRAM bytes per launch of `kernel` on this workload, scaled from the committed ncu
+    capture in profiles/dram_traffic.txt; None if the kernels changed since."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    try:
+        sha = kernel_source_sha()
+        with open(path) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) < 6 or parts[0].startswith("#") or parts[0] != kernel:
+                    continue
+                if parts[1] != sha or int(parts[3]) != nd:
+                    continue
+                return (int(parts[4]) + int(parts[5])) * psi / int(parts[2])
+    except (OSError, ValueError):
+        pass
+    return None
+
+
 def host_mem_available() -> int:
     try:
         with open("/proc/meminfo") as f:
@@ -305,8 +338,10 @@ def run_ours(args):
     if a_ms >= b_ms:
         kname, kms, kbytes = "k_reduce (fold + unscale + flag + norm partials, writes fp32 g)", \
             a_ms, (2 * nd + 4) * psi
+        traffic = ncu_traffic("k_reduce", psi, nd)
     else:
         kname, kms, kbytes = "k_update (clip + Adam + cast + write-back)", b_ms, 30 * psi
+        traffic = ncu_traffic("k_update", psi, nd)
     achieved = kbytes / (kms / 1e3) / 1e9
 
     out = {
@@ -325,7 +360,9 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak,
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind ==
                      "measured" else "fallback", "unit": "GB/s", "frac": achieved / peak,
-                     "algorithmic_bytes_per_launch": kbytes, "traffic": None},
+                     "algorithmic_bytes_per_launch": kbytes, "traffic": traffic,
+                     "traffic_source": "ncu dram bytes of a 64M-parameter capture scaled by "
+                                       "elements (profiles/dram_traffic.txt)" if traffic else None},
         "gpu_launches": launches,
         "clocks": clocks,
         "step_result": {k: res[k] for k in ("skipped", "grad_norm", "clip_coef", "loss_scale",
