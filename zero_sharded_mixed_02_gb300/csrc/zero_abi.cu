@@ -17,6 +17,7 @@ namespace {
 constexpr int PATH_FUSED = 0, PATH_G32 = 1, PATH_RECOMPUTE = 2;
 constexpr int PROFILE_RING = 256;
 constexpr uint64_t LAYOUT_ALIGN = 64;   // elements; keeps 16-byte vectors inside a shard
+constexpr uint64_t REDUCE_WAVES = 8;    // reduce/fused grid: waves of SMs x occupancy
 
 struct ProfileSlot {
     cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
@@ -41,7 +42,8 @@ struct zero_plan {
     int path = PATH_FUSED;
     const void* fn_a = nullptr;
     const void* fn_b = nullptr;
-    int grid_a = 1, grid_b = 1;
+    int grid_a = 1;
+    uint64_t grid_b = 1;
     uint64_t workspace = 0;
     // device
     int device = 0, sms = 1;
@@ -98,18 +100,25 @@ void destroy_plan(zero_plan* p)
     delete p;
 }
 
-// Largest grid the kernel keeps resident on every SM, capped by the work
-// (one thread per 8-element vector) and by the per-block partials array.
-int grid_for(const void* fn, int sms, uint64_t n)
+// Reduce and fused passes: REDUCE_WAVES waves of (SMs x resident blocks per SM),
+// capped by the work (one thread per 8-element vector) and by the per-block
+// partials array.
+int grid_reduce(const void* fn, int sms, uint64_t n)
 {
     int occ = 1;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, ZERO_THREADS, 0) != cudaSuccess ||
         occ < 1)
         occ = 1;
     const uint64_t want = std::max<uint64_t>(1, ceil_div(n / 8, ZERO_THREADS));
-    uint64_t g = std::min<uint64_t>((uint64_t)sms * (uint64_t)occ, want);
+    uint64_t g = std::min<uint64_t>((uint64_t)sms * (uint64_t)occ * REDUCE_WAVES, want);
     g = std::min<uint64_t>(g, ZERO_MAX_BLOCKS);
     return (int)std::max<uint64_t>(g, 1);
+}
+
+// Update pass: one thread per 4 elements (the last slot may be partial).
+uint64_t grid_update(uint64_t n)
+{
+    return std::max<uint64_t>(1, ceil_div(ceil_div(n, 4), ZERO_THREADS));
 }
 
 zero_status_t create_impl(uint64_t psi, int nd, int stage, zero_dtype_t dtype,
@@ -229,8 +238,12 @@ zero_status_t create_impl(uint64_t psi, int nd, int stage, zero_dtype_t dtype,
         destroy_plan(p);
         return ZERO_ECUDA;
     }
-    p->grid_a = grid_for(p->fn_a, p->sms, p->n);
-    p->grid_b = p->fn_b ? grid_for(p->fn_b, p->sms, p->n) : 1;
+    p->grid_a = grid_reduce(p->fn_a, p->sms, p->n);
+    p->grid_b = grid_update(p->n);
+    if (p->grid_b > 0x7FFFFFFFull) {
+        destroy_plan(p);
+        return ZERO_EINVAL;
+    }
 
     if (cudaMalloc(&p->d_state, sizeof(DevState)) != cudaSuccess ||
         cudaMallocHost(&p->h_mirror, sizeof(DevScalars) + sizeof(DevStatus)) != cudaSuccess) {
@@ -394,7 +407,7 @@ zero_status_t zero_step(zero_plan_t plan, const void* grads, float* master, floa
     plan->launches++;
     if (slot && cudaEventRecord(slot->ev[1], s) != cudaSuccess) return ZERO_ECUDA;
     if (plan->fn_b) {
-        e = cudaLaunchKernel(plan->fn_b, dim3(plan->grid_b), dim3(ZERO_THREADS), args, 0, s);
+        e = cudaLaunchKernel(plan->fn_b, dim3((unsigned)plan->grid_b), dim3(ZERO_THREADS), args, 0, s);
         if (e != cudaSuccess) return ZERO_ECUDA;
         plan->launches++;
     }

@@ -1,11 +1,12 @@
 // zero_step_kernels.cuh -- the optimizer-step kernels (templates).
 //
-// Grid: a persistent grid of ZERO_THREADS-thread blocks, sized once per plan
-// from the SM count and the kernel's occupancy.  Thread t of block b handles
-// the 8-element vectors b*T + t, b*T + t + G*T, ... (static assignment), so the
-// per-block sums of squares and their fixed-order combination are the same on
-// every run.  The last block to finish (an atomic ticket, no waiting) combines
-// the per-block partials in block order and writes the step status.
+// Reduce and fused passes: a grid of ZERO_THREADS-thread blocks, a few waves of
+// the SM count times the kernel's occupancy, sized once per plan.  Thread t of
+// block b handles the 8-element vectors b*T + t, b*T + t + G*T, ... (static
+// assignment), so the per-block sums of squares and their fixed-order
+// combination are the same on every run.  The last block to finish (an atomic
+// ticket, no waiting) combines the per-block partials in block order and
+// writes the step status.  The update pass uses one thread per 4 elements.
 #pragma once
 
 #include "zero_common.cuh"
@@ -154,52 +155,46 @@ __global__ void __launch_bounds__(ZERO_THREADS) k_reduce(const StepArgs a)
 }
 
 // ---- pass 2: stages 4-6a (clip, Adam, cast, write-back) -------------------
+// One thread per 4 consecutive elements, one launch-wide block per 1024
+// elements (not a persistent grid: measured faster for this read-write mix).
+// The thread whose 4-element slot runs past n takes the ragged tail alone.
 template <int DT, int ND, bool RECOMPUTE>
 __global__ void __launch_bounds__(ZERO_THREADS) k_update(const StepArgs a)
 {
     const DevStatus st = a.state->st;
     if (st.skipped) return;
     const int nd = ND > 0 ? ND : a.nd;
-    Unscale un;
-    un.init(nd, st.used_scale);
     const float c = st.clip_coef, bc1 = st.bc1, bc2 = st.bc2;
-    const int64_t nvec = a.n >> 3;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    float4* pm = reinterpret_cast<float4*>(a.master);
-    float4* mm = reinterpret_cast<float4*>(a.m);
-    float4* vv = reinterpret_cast<float4*>(a.v);
-    for (int64_t vi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; vi < nvec; vi += stride) {
-        float g[8], p[8], m[8], v[8];
-        const float4 p0 = __ldcs(pm + 2 * vi), p1 = __ldcs(pm + 2 * vi + 1);
-        const float4 m0 = __ldcs(mm + 2 * vi), m1 = __ldcs(mm + 2 * vi + 1);
-        const float4 v0 = __ldcs(vv + 2 * vi), v1 = __ldcs(vv + 2 * vi + 1);
+    const int64_t vi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t nvec = a.n >> 2;
+    Unscale un;
+    if (RECOMPUTE) un.init(nd, st.used_scale);
+    if (vi < nvec) {
+        float4* pm = reinterpret_cast<float4*>(a.master) + vi;
+        float4* mm = reinterpret_cast<float4*>(a.m) + vi;
+        float4* vv = reinterpret_cast<float4*>(a.v) + vi;
+        float4 p = __ldcs(pm), m = __ldcs(mm), v = __ldcs(vv);
+        float g[4];
         if (RECOMPUTE) {
-            float s[8];
-            fold8<DT, ND>(a.grads, a.rank_stride, vi, nd, s);
+            float s[4];
+            fold4<DT, ND>(a.grads, a.rank_stride, vi, nd, s);
 #pragma unroll
-            for (int e = 0; e < 8; e++) g[e] = un(s[e]);
+            for (int e = 0; e < 4; e++) g[e] = un(s[e]);
         } else {
-            const float4* gv = reinterpret_cast<const float4*>(a.g32) + 2 * vi;
-            unpack8(__ldcs(gv), __ldcs(gv + 1), g);
+            const float4 g4 = __ldcs(reinterpret_cast<const float4*>(a.g32) + vi);
+            g[0] = g4.x; g[1] = g4.y; g[2] = g4.z; g[3] = g4.w;
         }
-        unpack8(p0, p1, p);
-        unpack8(m0, m1, m);
-        unpack8(v0, v1, v);
-#pragma unroll
-        for (int e = 0; e < 8; e++) adam1(g[e], c, p[e], m[e], v[e], bc1, bc2, a.k);
-        __stcs(pm + 2 * vi, make_float4(p[0], p[1], p[2], p[3]));
-        __stcs(pm + 2 * vi + 1, make_float4(p[4], p[5], p[6], p[7]));
-        __stcs(mm + 2 * vi, make_float4(m[0], m[1], m[2], m[3]));
-        __stcs(mm + 2 * vi + 1, make_float4(m[4], m[5], m[6], m[7]));
-        __stcs(vv + 2 * vi, make_float4(v[0], v[1], v[2], v[3]));
-        __stcs(vv + 2 * vi + 1, make_float4(v[4], v[5], v[6], v[7]));
-        __stcs(reinterpret_cast<uint4*>(a.params) + vi,
-               make_uint4(narrow2<DT>(p[0], p[1]), narrow2<DT>(p[2], p[3]),
-                          narrow2<DT>(p[4], p[5]), narrow2<DT>(p[6], p[7])));
-    }
-    if (blockIdx.x == 0 && threadIdx.x < 8) {
-        const int64_t i = (nvec << 3) + threadIdx.x;
-        if (i < a.n) {
+        adam1(g[0], c, p.x, m.x, v.x, bc1, bc2, a.k);
+        adam1(g[1], c, p.y, m.y, v.y, bc1, bc2, a.k);
+        adam1(g[2], c, p.z, m.z, v.z, bc1, bc2, a.k);
+        adam1(g[3], c, p.w, m.w, v.w, bc1, bc2, a.k);
+        __stcs(pm, p);
+        __stcs(mm, m);
+        __stcs(vv, v);
+        __stcs(reinterpret_cast<uint2*>(a.params) + vi,
+               make_uint2(narrow2<DT>(p.x, p.y), narrow2<DT>(p.z, p.w)));
+    } else if (vi == nvec) {
+        for (int64_t i = nvec << 2; i < a.n; i++) {
             const float g = RECOMPUTE ? un(fold1<DT>(a.grads, a.rank_stride, i, nd)) : a.g32[i];
             float p = a.master[i], m = a.m[i], v = a.v[i];
             adam1(g, c, p, m, v, bc1, bc2, a.k);
