@@ -274,6 +274,8 @@ def run_ours(args):
                    decoupled_wd=w.decoupled_wd, clip_norm=w.clip, loss_scale=w.loss_scale,
                    dynamic_scale=w.dynamic_scale, backoff=0.5, growth_interval=1000)
     plan = z.zero_plan_create(w.psi, w.nd, w.stage, w.dtype, w.shapes, hp)
+    if args.reduce_kernel == "tma":
+        z.zero_plan_set_reduce_kernel(plan, z.REDUCE_TMA)
     shard, padded, _, ws_bytes = z.zero_plan_layout(plan)
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
@@ -363,6 +365,7 @@ def run_ours(args):
                      "algorithmic_bytes_per_launch": kbytes, "traffic": traffic,
                      "traffic_source": "ncu dram bytes of a 64M-parameter capture scaled by "
                                        "elements (profiles/dram_traffic.txt)" if traffic else None},
+        "reduce_kernel": args.reduce_kernel,
         "gpu_launches": launches,
         "clocks": clocks,
         "step_result": {k: res[k] for k in ("skipped", "grad_norm", "clip_coef", "loss_scale",
@@ -463,6 +466,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=1 << 23)
     ap.add_argument("--ref-sample", type=int, default=1 << 21)
+    ap.add_argument("--reduce-kernel", choices=("ldg", "tma"), default="ldg",
+                    help="reduce-pass kernel: 128-bit loads (default) or TMA bulk staging")
     ap.add_argument("--psi", type=int, default=0,
                     help="flat model of this many parameters (profiling small cases)")
     args = ap.parse_args(argv)

@@ -34,7 +34,7 @@
  *   - Ownership: the caller allocates and owns every device buffer and the
  *     stream; the library borrows raw device pointers for the duration of a
  *     call.  A plan owns only its host bookkeeping and a small device block
- *     (optimizer scalars, step status, per-block partials: a few tens of KB,
+ *     (optimizer scalars, step status, per-block partials: about 100 KB,
  *     allocated by zero_plan_create on the current device).
  *   - Device pointers must be 16-byte aligned.  Streams are cudaStream_t
  *     passed as void* (NULL = the legacy default stream).
@@ -253,6 +253,17 @@ zero_status_t zero_plan_kernel_times(zero_plan_t plan, double* reduce_ms, double
  * scale), 1 = two passes through an fp32 gradient in the workspace, 2 = two
  * passes that re-read the 16-bit gradients (clip or dynamic scale, nd < 4). */
 int zero_plan_path(zero_plan_t plan);
+
+/* Which kernel runs the reduce pass of a two-pass plan: 0 = 128-bit loads of
+ * the rank rows (the default, measured fastest at nd = 16), 1 = TMA bulk
+ * staging (cp.async.bulk of each rank's 2 KB row slice into a ring of shared-
+ * memory stages, a producer warp and eight consumer warps).  Both compute the
+ * same reduced gradient bit for bit; the norm's partial sums are grouped
+ * differently.  Kind 1 needs the two-pass path with the fp32 workspace and
+ * 4 <= nd <= 48 (ZERO_EINVAL otherwise).  Waits for the plan's last step.
+ * A bounded wait in kind 1 that gives up makes zero_step_result return
+ * ZERO_ETIMEOUT from then on. */
+zero_status_t zero_plan_set_reduce_kernel(zero_plan_t plan, int kind);
 
 #ifdef __cplusplus
 }

@@ -143,12 +143,14 @@ def stage3_valid_mask(z, plan, nd, rank=0):
     return mask
 
 
-def run_gpu(z, c: Case, keep_g32=False, plan_out=None) -> Run:
+def run_gpu(z, c: Case, keep_g32=False, plan_out=None, reduce_kernel=0) -> Run:
     import torch
     dev = torch.device("cuda", 0)
     plan = z.zero_plan_create(c.psi, c.nd, c.stage, c.dtype, c.shapes, c.hparams(z),
                               units=c.units if c.stage == 3 else None)
     try:
+        if reduce_kernel:
+            z.zero_plan_set_reduce_kernel(plan, reduce_kernel)
         shard, padded, nunits, ws = z.zero_plan_layout(plan)
         n = c.psi if c.stage <= 2 else padded
         mask = stage3_valid_mask(z, plan, c.nd) if c.stage == 3 else None

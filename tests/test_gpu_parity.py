@@ -26,8 +26,8 @@ def z():
     return z
 
 
-def check(z, c, bit_exact=False, g32=False):
-    gpu = H.run_gpu(z, c, keep_g32=g32)
+def check(z, c, bit_exact=False, g32=False, reduce_kernel=0):
+    gpu = H.run_gpu(z, c, keep_g32=g32, reduce_kernel=reduce_kernel)
     n = gpu.master.size
     padded = n
     if c.stage <= 2:
@@ -227,3 +227,29 @@ def test_profile_counts_kernels(z):
         assert z.zero_plan_path(plan) == z.PATH_G32
     finally:
         z.zero_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("psi,nd,dtype", [(1_000_003, 16, gen.FP16), (4096 * 7, 5, gen.BF16),
+                                          (1000, 4, gen.FP16), (300_000, 32, gen.BF16),
+                                          (1 << 20, 8, gen.FP16), (2048 + 8, 48, gen.BF16)])
+def test_tma_staged_reduce(z, psi, nd, dtype):
+    # the reduce pass with TMA bulk staging of the rank rows: same reduced gradient
+    # bit for bit, same flags and skips; sizes below, at and off the 1024-element tile
+    if dtype == gen.FP16:
+        c = H.Case(shapes=[(psi,)], nd=nd, dtype=dtype, grad_sigma=1e-3, loss_scale=2048.0,
+                   dynamic_scale=1, clip=1.0, steps=4, inf_steps=(2,))
+    else:
+        c = H.Case(shapes=[(psi,)], nd=nd, clip=0.5, steps=3, weight_decay=0.01)
+    check(z, c, g32=True, reduce_kernel=1)
+
+
+def test_tma_staged_reduce_rejects_unsupported(z):
+    for nd, kw in ((2, dict(clip=1.0)), (8, dict()), (64, dict(clip=1.0))):
+        c = H.Case(shapes=[(4096,)], nd=nd, **kw)
+        plan = z.zero_plan_create(c.psi, c.nd, 2, c.dtype, c.shapes, c.hparams(z))
+        try:
+            with pytest.raises(z.ZeroError):
+                z.zero_plan_set_reduce_kernel(plan, 1)
+            z.zero_plan_set_reduce_kernel(plan, 0)
+        finally:
+            z.zero_plan_destroy(plan)

@@ -32,7 +32,7 @@ ENTRY_POINTS = (
     "zero_plan_unit", "zero_step", "zero_step_result", "zero_step_overflow",
     "zero_gather_layer", "zero_state_bytes", "zero_comm_volume", "zero_max_params",
     "zero_status_string", "zero_plan_profile", "zero_plan_kernel_times", "zero_plan_path",
-    "zero_grad_norm_noalloc",
+    "zero_grad_norm_noalloc", "zero_plan_set_reduce_kernel",
 )
 
 
@@ -98,6 +98,7 @@ def lib():
                 "zero_plan_path": (ctypes.c_int, [_P]),
                 "zero_grad_norm_noalloc": (st, [_P, ctypes.c_int, _U64, _U64, ctypes.c_int,
                                                 ctypes.c_float, _P, _P, _P]),
+                "zero_plan_set_reduce_kernel": (st, [_P, ctypes.c_int]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -177,6 +178,13 @@ def zero_plan_unit(plan: int, unit: int) -> Tuple[int, int, int]:
 
 def zero_plan_path(plan: int) -> int:
     return lib().zero_plan_path(plan)
+
+
+REDUCE_LDG, REDUCE_TMA = 0, 1
+
+
+def zero_plan_set_reduce_kernel(plan: int, kind: int) -> None:
+    _check(lib().zero_plan_set_reduce_kernel(plan, kind), "zero_plan_set_reduce_kernel")
 
 
 def zero_step(plan: int, grads, master, m, v, params, workspace=None, stream=0) -> None:

@@ -17,7 +17,10 @@ namespace {
 constexpr int PATH_FUSED = 0, PATH_G32 = 1, PATH_RECOMPUTE = 2;
 constexpr int PROFILE_RING = 256;
 constexpr uint64_t LAYOUT_ALIGN = 64;   // elements; keeps 16-byte vectors inside a shard
-constexpr uint64_t REDUCE_WAVES = 8;    // reduce/fused grid: waves of SMs x occupancy
+constexpr uint64_t REDUCE_WAVES = 12;   // reduce grid: waves of SMs x occupancy (measured)
+constexpr uint64_t FUSED_WAVES = 8;     // fused single-pass grid
+constexpr uint64_t TMA_STAGE_BUDGET = 131072;  // bytes of staged rows per CTA (4 stages at nd 16)
+constexpr uint64_t TMA_SMEM_MAX = 196608;      // largest ring of stages a CTA may hold
 
 struct ProfileSlot {
     cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
@@ -43,6 +46,10 @@ struct zero_plan {
     const void* fn_a = nullptr;
     const void* fn_b = nullptr;
     int grid_a = 1;
+    int block_a = ZERO_THREADS;
+    size_t smem_a = 0;              // dynamic shared memory of the reduce pass
+    int reduce_kernel = 0;          // 0: 128-bit loads; 1: TMA bulk staging
+    int tma_stages = 0;
     uint64_t grid_b = 1;
     uint64_t workspace = 0;
     // device
@@ -100,17 +107,17 @@ void destroy_plan(zero_plan* p)
     delete p;
 }
 
-// Reduce and fused passes: REDUCE_WAVES waves of (SMs x resident blocks per SM),
+// Reduce and fused passes: `waves` waves of (SMs x resident blocks per SM),
 // capped by the work (one thread per 8-element vector) and by the per-block
 // partials array.
-int grid_reduce(const void* fn, int sms, uint64_t n)
+int grid_reduce(const void* fn, int sms, uint64_t n, uint64_t waves)
 {
     int occ = 1;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, ZERO_THREADS, 0) != cudaSuccess ||
         occ < 1)
         occ = 1;
     const uint64_t want = std::max<uint64_t>(1, ceil_div(n / 8, ZERO_THREADS));
-    uint64_t g = std::min<uint64_t>((uint64_t)sms * (uint64_t)occ * REDUCE_WAVES, want);
+    uint64_t g = std::min<uint64_t>((uint64_t)sms * (uint64_t)occ * waves, want);
     g = std::min<uint64_t>(g, ZERO_MAX_BLOCKS);
     return (int)std::max<uint64_t>(g, 1);
 }
@@ -238,7 +245,8 @@ zero_status_t create_impl(uint64_t psi, int nd, int stage, zero_dtype_t dtype,
         destroy_plan(p);
         return ZERO_ECUDA;
     }
-    p->grid_a = grid_reduce(p->fn_a, p->sms, p->n);
+    p->grid_a = grid_reduce(p->fn_a, p->sms, p->n,
+                            p->path == PATH_FUSED ? FUSED_WAVES : REDUCE_WAVES);
     p->grid_b = grid_update(p->n);
     if (p->grid_b > 0x7FFFFFFFull) {
         destroy_plan(p);
@@ -361,6 +369,44 @@ zero_status_t zero_plan_unit(zero_plan_t plan, int unit, uint64_t* len, uint64_t
 
 int zero_plan_path(zero_plan_t plan) { return plan ? plan->path : -1; }
 
+zero_status_t zero_plan_set_reduce_kernel(zero_plan_t plan, int kind)
+{
+    if (!plan || (kind != 0 && kind != 1)) return ZERO_EINVAL;
+    if (plan->stepped && cudaEventSynchronize(plan->ev_done) != cudaSuccess) return ZERO_ECUDA;
+    if (kind == 0) {
+        plan->fn_a = step_kernel((int)plan->dtype, plan->path == PATH_FUSED ? K_FUSED
+                                 : plan->path == PATH_G32 ? K_REDUCE_G32 : K_REDUCE_ONLY,
+                                 plan->nd);
+        plan->grid_a = grid_reduce(plan->fn_a, plan->sms, plan->n,
+                                   plan->path == PATH_FUSED ? FUSED_WAVES : REDUCE_WAVES);
+        plan->block_a = ZERO_THREADS;
+        plan->smem_a = 0;
+        plan->tma_stages = 0;
+        plan->reduce_kernel = 0;
+        return ZERO_OK;
+    }
+    // TMA staging: the two-pass path, with a ring of at least two stages of
+    // nd rows x 2 KB that fits in one CTA's shared memory
+    const uint64_t stage = (uint64_t)plan->nd * 2 * 1024;
+    if (plan->path != PATH_G32 || 2 * stage > TMA_SMEM_MAX) return ZERO_EINVAL;
+    // the same rule as tma_stages_for(): ~128 KB of rows, 2..8 stages
+    uint64_t stages = std::max<uint64_t>(2, TMA_STAGE_BUDGET / stage);
+    stages = std::min<uint64_t>(stages, 8);
+    const void* fn = step_kernel((int)plan->dtype, K_REDUCE_G32_TMA, plan->nd);
+    if (!fn) return ZERO_EINVAL;
+    const size_t smem = (size_t)(stages * stage);
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+        return ZERO_ECUDA;
+    plan->fn_a = fn;
+    plan->grid_a = std::min(plan->sms, ZERO_MAX_BLOCKS);
+    plan->block_a = 288;
+    plan->smem_a = smem;
+    plan->tma_stages = (int)stages;
+    plan->reduce_kernel = 1;
+    return ZERO_OK;
+}
+
 zero_status_t zero_step(zero_plan_t plan, const void* grads, float* master, float* m, float* v,
                         void* params, void* workspace, void* stream)
 {
@@ -401,8 +447,11 @@ zero_status_t zero_step(zero_plan_t plan, const void* grads, float* master, floa
         plan->ring_pos++;
         if (cudaEventRecord(slot->ev[0], s) != cudaSuccess) return ZERO_ECUDA;
     }
+    int stages = plan->tma_stages;
+    void* args_tma[] = {&a, &stages};
     void* args[] = {&a};
-    cudaError_t e = cudaLaunchKernel(plan->fn_a, dim3(plan->grid_a), dim3(ZERO_THREADS), args, 0, s);
+    cudaError_t e = cudaLaunchKernel(plan->fn_a, dim3(plan->grid_a), dim3(plan->block_a),
+                                     plan->reduce_kernel ? args_tma : args, plan->smem_a, s);
     if (e != cudaSuccess) return ZERO_ECUDA;
     plan->launches++;
     if (slot && cudaEventRecord(slot->ev[1], s) != cudaSuccess) return ZERO_ECUDA;
@@ -434,7 +483,7 @@ zero_status_t zero_step_result(zero_plan_t plan, int* skipped, double* grad_norm
     if (clip_coef) *clip_coef = st->clip_coef;
     if (loss_scale) *loss_scale = sc->loss_scale;
     if (t) *t = sc->t;
-    return ZERO_OK;
+    return st->err ? ZERO_ETIMEOUT : ZERO_OK;
 }
 
 zero_status_t zero_step_overflow(zero_plan_t plan, int* overflow)

@@ -47,7 +47,7 @@ static __device__ __noinline__ void finalize(const StepArgs a, double sumsq, int
     st.grad_norm  = __dsqrt_rn(sumsq);
     st.clip_coef  = (a.clip > 0.0f && st.grad_norm > (double)a.clip)
                         ? __double2float_rn(__ddiv_rn((double)a.clip, st.grad_norm)) : 1.0f;
-    st.err = 0;
+    st.err = S->st.err;        // sticky: a bounded wait that gave up, in any step
     st.pad = 0;
     if (overflow && a.dynamic) {
         st.skipped = 1;
@@ -116,8 +116,10 @@ static __device__ __forceinline__ void unpack8(const float4 a, const float4 b, f
 }
 
 // ---- pass 1: stages 1-3a (fold, average, unscale, flag, squares) ----------
+// At most 4 resident blocks per SM leaves each thread the registers to keep
+// all 16 rank loads of a chunk in flight (measured fastest).
 template <int DT, int ND, bool WRITE_G>
-__global__ void __launch_bounds__(ZERO_THREADS) k_reduce(const StepArgs a)
+__global__ void __launch_bounds__(ZERO_THREADS, 4) k_reduce(const StepArgs a)
 {
     __shared__ RedShared sh;
     const int nd = ND > 0 ? ND : a.nd;
@@ -162,7 +164,7 @@ template <int DT, int ND, bool RECOMPUTE>
 __global__ void __launch_bounds__(ZERO_THREADS) k_update(const StepArgs a)
 {
     const DevStatus st = a.state->st;
-    if (st.skipped) return;
+    if (st.skipped || st.err) return;
     const int nd = ND > 0 ? ND : a.nd;
     const float c = st.clip_coef, bc1 = st.bc1, bc2 = st.bc2;
     const int64_t vi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;

@@ -5,6 +5,7 @@
 
 #include "zero_launch.h"
 #include "zero_step_kernels.cuh"
+#include "zero_tma.cuh"
 
 namespace zero {
 
@@ -31,6 +32,15 @@ static const void* fused_or_reduce(int kind)
 template <int DT>
 static const void* step_kernel_dt(int kind, int nd)
 {
+    if (kind == K_REDUCE_G32_TMA) {
+        switch (nd) {
+        case 4:  return (const void*)k_reduce_tma<DT, 4>;
+        case 8:  return (const void*)k_reduce_tma<DT, 8>;
+        case 16: return (const void*)k_reduce_tma<DT, 16>;
+        case 32: return (const void*)k_reduce_tma<DT, 32>;
+        default: return (const void*)k_reduce_tma<DT, 0>;
+        }
+    }
     switch (nd) {
     case 1:  return fused_or_reduce<DT, 1>(kind);
     case 2:  return fused_or_reduce<DT, 2>(kind);
