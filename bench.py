@@ -88,7 +88,7 @@ def measured_peaks():
 
 
 KERNEL_SOURCES = ("zero_common.cuh", "zero_step_kernels.cuh", "zero_step_table.cuh",
-                  "zero_step_fp16.cu", "zero_step_bf16.cu")
+                  "zero_step_fp16.cu", "zero_step_bf16.cu", "zero_tma.cuh")
 
 
 def kernel_source_sha() -> str:

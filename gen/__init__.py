@@ -128,6 +128,21 @@ def ranks_16(seed, stream, step, nd, n, sigma, scale=1.0, dtype=FP16, rank_strid
     return out
 
 
+def ranks_16_mt(seed, stream, step, nd, n, sigma, scale=1.0, dtype=FP16, rank_stride=None,
+                index0=0, nthreads=None):
+    """ranks_16 with one host thread per rank row (same bits)."""
+    import concurrent.futures
+    rs = n if rank_stride is None else rank_stride
+    out = np.zeros((nd, rs), np.uint16)
+    L, k = host(), kappa(sigma)
+
+    def row(r):
+        L.zgen_16(seed, stream, step, r, index0, n, k, scale, dtype, out[r].ctypes.data)
+    with concurrent.futures.ThreadPoolExecutor(nthreads or min(nd, os.cpu_count() or 1)) as ex:
+        list(ex.map(row, range(nd)))
+    return out
+
+
 def f32(seed, stream, step, rank, n, sigma, scale=1.0, index0=0):
     out = np.empty(n, np.float32)
     host().zgen_f32(seed, stream, step, rank, index0, n, kappa(sigma), scale, _ptr(out))

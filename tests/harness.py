@@ -107,8 +107,8 @@ def grads_for_step(c: Case, step: int, n: int, rank_stride: int, scale: float,
                    valid_mask: Optional[np.ndarray] = None) -> np.ndarray:
     """[nd][rank_stride] 16-bit gradients of step `step` (1-based), generated with
     the loss scale in force; +inf / NaN planted on the overflow steps."""
-    g = gen.ranks_16(c.seed, gen.STREAM_GRAD, step, c.nd, n, c.grad_sigma, scale, c.dtype,
-                     rank_stride=rank_stride)
+    g = gen.ranks_16_mt(c.seed, gen.STREAM_GRAD, step, c.nd, n, c.grad_sigma, scale, c.dtype,
+                        rank_stride=rank_stride)
     if valid_mask is not None:
         g[:, :n][:, ~valid_mask] = 0
     for steps, bits in ((c.inf_steps, 0x7C00 if c.dtype == gen.FP16 else 0x7F80),
@@ -229,3 +229,64 @@ def compare_runs(gpu: Run, ora: Run, what=""):
             assert not np.isfinite(a["grad_norm"])
     assert_state_close((gpu.master, gpu.m, gpu.v, gpu.params),
                        (ora.master, ora.m, ora.v, ora.params), what)
+
+
+# ------------------------------------------------------- full-size helpers
+def oracle_norm_streamed(seed, step, nd, n, sigma, scale, dtype, inf_at=None, nthreads=None,
+                         chunk=1 << 21, index_map=None):
+    """The oracle's global norm and overflow flag over n elements whose gradients
+    are too many to hold at once: the flat vector is cut into contiguous ranges
+    (one per host thread, like ranks of the sharded oracle), each range streamed
+    in chunks through oracle.reduce / oracle.sumsq, and the range partials added
+    in range order.  inf_at = (rank, index) plants +inf there."""
+    import concurrent.futures
+    import os
+    nthreads = nthreads or min(os.cpu_count() or 1, 32)
+    bounds = [n * k // nthreads for k in range(nthreads + 1)]
+    inf_bits = 0x7C00 if dtype == gen.FP16 else 0x7F80
+
+    def work(k):
+        lo, hi = bounds[k], bounds[k + 1]
+        part, ovf = 0.0, False
+        for a in range(lo, hi, chunk):
+            b = min(a + chunk, hi)
+            g16 = gen.ranks_16(seed, gen.STREAM_GRAD, step, nd, b - a, sigma, scale, dtype,
+                               index0=a)
+            if inf_at is not None and a <= inf_at[1] < b:
+                g16[inf_at[0], inf_at[1] - a] = inf_bits
+            g, o = oracle.reduce(nd, dtype, g16, loss_scale=scale)
+            ovf = ovf or o
+            part = part + oracle.sumsq(g)
+        return part, ovf
+
+    with concurrent.futures.ThreadPoolExecutor(nthreads) as ex:
+        parts = list(ex.map(work, range(nthreads)))
+    total = 0.0
+    ovf = False
+    for p, o in parts:
+        total = total + p
+        ovf = ovf or o
+    return float(np.sqrt(total)), ovf
+
+
+def sample_indices(n, shard, nd, k=1 << 16, seed=1):
+    rng = np.random.default_rng(seed)
+    idx = set(rng.integers(0, n, k).tolist())
+    for r in range(nd + 1):
+        for d in (-1, 0, 1):
+            j = r * shard + d
+            if 0 <= j < n:
+                idx.add(j)
+    idx.update(range(max(0, n - 9), n))
+    idx.update(range(min(n, 9)))
+    return np.array(sorted(idx), np.int64)
+
+
+def oracle_sampled_grads(seed, step, nd, idx, sigma, scale, dtype, inf_at=None):
+    g16 = np.stack([gen.s16_at(seed, gen.STREAM_GRAD, step, r, idx, sigma, scale, dtype)
+                    for r in range(nd)])
+    if inf_at is not None:
+        hit = np.flatnonzero(idx == inf_at[1])
+        if hit.size:
+            g16[inf_at[0], hit[0]] = 0x7C00 if dtype == gen.FP16 else 0x7F80
+    return g16
