@@ -200,26 +200,52 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------- workload
-def workload(psi=None):
-    """The GPT-2 1.5B workload; with psi, a flat single-tensor model of psi
-    parameters under the same settings (small cases for profiling)."""
+WORKLOADS = ("gpt2-1.5b", "gpt2-small", "tiny", "llama3-8b")
+
+
+def metric_of(w):
+    if w.name == "gpt2-1.5b":
+        return METRIC
+    return f"sharded Adam step params/s and HBM GB/s vs GB300 peak ({w.name}, Nd={w.nd})"
+
+
+def workload(psi=None, name="gpt2-1.5b"):
+    """The GPT-2 1.5B workload (default) or another named one; with psi, a flat
+    single-tensor model of psi parameters under the same settings (small cases
+    for profiling)."""
     import dataclasses
     from gen import workloads
-    w = workloads.gpt2_xl()
+    w = {"gpt2-1.5b": workloads.gpt2_xl, "gpt2-small": workloads.gpt2_small,
+         "tiny": workloads.tiny, "llama3-8b": workloads.llama3_8b}[name]()
     if psi:
         w = dataclasses.replace(w, name=f"flat-{psi}", shapes=[(psi,)])
     return w
 
 
+DESCRIPTIONS = {
+    "gpt2-1.5b": "GPT-2 1.5B parameter list (48 layers, h=1600, ffn=6400, vocab 50257, ctx 1024)",
+    "gpt2-small": "GPT-2 small parameter list (12 layers, h=768, ffn=3072, vocab 50257, ctx 1024)",
+    "tiny-flat-4t": "tiny flat model: 4 tensors [512x1024, 1024, 1024x512, 512]",
+    "llama3-8b": "LLaMA-3-8B parameter list (32 layers, h=4096, ffn=14336, 32q/8kv, vocab 128256)",
+}
+
+
 def config_of(w, padded):
-    desc = (f"{w.name}: GPT-2 1.5B parameter list (48 layers, h=1600, ffn=6400, vocab 50257, "
-            f"ctx 1024), {len(w.shapes)} tensors" if len(w.shapes) > 1 else
-            f"{w.name}: one flat tensor of {w.psi} parameters, GPT-2 1.5B settings")
+    desc = (f"{w.name}: {DESCRIPTIONS.get(w.name, w.name)}, {len(w.shapes)} tensors"
+            if len(w.shapes) > 1 else
+            f"{w.name}: one flat tensor of {w.psi} parameters, {w.nd} ranks")
     return {"workload": desc,
             "psi": w.psi, "nd": w.nd, "zero_stage": w.stage, "padded_elems": padded,
-            "grads": "fp16 N(0,1e-3) x 65536 loss scale (dynamic)", "clip_norm": w.clip,
-            "optimizer": "Adam lr 1e-3 betas (0.9, 0.999) eps 1e-8",
-            "l2": "inputs (~78 GB resident) far larger than the 129 MB L2; no flush needed",
+            "grads": (f"{'fp16' if w.dtype == 0 else 'bf16'} N(0,{w.grad_sigma:g})"
+                      + (f" x {w.loss_scale:g} loss scale" if w.loss_scale != 1 else "")
+                      + (" (dynamic)" if w.dynamic_scale else "")),
+            "clip_norm": w.clip,
+            "optimizer": (f"{'AdamW' if w.weight_decay else 'Adam'} lr {w.lr:g} betas "
+                          f"({w.beta1:g}, {w.beta2:g}) eps {w.eps:g}"
+                          + (f" wd {w.weight_decay:g}" if w.weight_decay else "")),
+            "l2": (f"inputs ({(2 * w.nd + 14) * padded / 1e9:.1f} GB resident) vs the 129 MB L2"
+                   + ("; larger, no flush needed" if (2 * w.nd + 14) * padded > (1 << 30) else
+                      "; smaller than 1 GB: timings include L2 reuse")),
             "parallelism": "Nd ranks emulated in one GPU's HBM"}
 
 
@@ -269,7 +295,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     zbuild.build()
-    w = workload(args.psi)
+    w = workload(args.psi, args.workload)
     hp = z.hparams(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
                    decoupled_wd=w.decoupled_wd, clip_norm=w.clip, loss_scale=w.loss_scale,
                    dynamic_scale=w.dynamic_scale, backoff=0.5, growth_interval=1000)
@@ -347,10 +373,10 @@ def run_ours(args):
     achieved = kbytes / (kms / 1e3) / 1e9
 
     out = {
-        "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": ws, "steps": K,
+        "metric": metric_of(w), "value": value, "unit": "params/s", "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic (seeded counter-based generator; GPT-2 1.5B shape list, no weights)",
+        "data": "synthetic (seeded counter-based generator; shape list only, no weights)",
         "config": config_of(w, padded),
         "hbm_gbs_roofline_bytes": step_gbs,
         "roofline_bytes_per_elem": 2 * nd + 26,
@@ -408,15 +434,32 @@ def e2e_leg(args, z, plan, w, grads, master, m, v, params, work, dev, stream):
     host.copy_(grads)
     sp = stream.cuda_stream
     K = max(3, min(args.steps, args.e2e_steps))
+    # the host->device copy is split by rank rows over several copy streams, which
+    # the step's stream then waits for
+    ns = max(1, min(args.e2e_streams, grads.shape[0]))
+    copy_streams = [torch.cuda.Stream(dev) for _ in range(ns)]
+    rows = [(grads.shape[0] * k // ns, grads.shape[0] * (k + 1) // ns) for k in range(ns)]
+
+    def h2d():
+        ready = torch.cuda.Event()
+        ready.record(stream)
+        for cs, (a, b) in zip(copy_streams, rows):
+            cs.wait_event(ready)
+            with torch.cuda.stream(cs):
+                grads[a:b].copy_(host[a:b], non_blocking=True)
+            done = torch.cuda.Event()
+            done.record(cs)
+            stream.wait_event(done)
+
     for _ in range(2):
-        grads.copy_(host, non_blocking=True)
+        h2d()
         z.zero_step(plan, grads, master, m, v, params, work, sp)
         z.zero_step_result(plan)
     barrier(dev)
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
     for _ in range(K):
-        grads.copy_(host, non_blocking=True)
+        h2d()
         z.zero_step(plan, grads, master, m, v, params, work, sp)
         z.zero_step_result(plan)
     torch.cuda.synchronize(dev)
@@ -424,7 +467,153 @@ def e2e_leg(args, z, plan, w, grads, master, m, v, params, work, dev, stream):
     _, _, ws = dist_env()
     del host
     return {"value": w.psi * K * ws / dt, "unit": "params/s", "h2d_bytes_per_step": nbytes,
-            "d2h_bytes_per_step": STATUS_BYTES, "steps": K, "ms_per_step": dt / K * 1e3}
+            "d2h_bytes_per_step": STATUS_BYTES, "steps": K, "ms_per_step": dt / K * 1e3,
+            "h2d_gbs": nbytes / (dt / K) / 1e9, "copy_streams": ns}
+
+
+# ------------------------------------------------------------ sweep and ZeRO-3
+def _plan_for(z, w, units=None):
+    hp = z.hparams(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
+                   decoupled_wd=w.decoupled_wd, clip_norm=w.clip, loss_scale=w.loss_scale,
+                   dynamic_scale=w.dynamic_scale, backoff=0.5, growth_interval=1000)
+    return z.zero_plan_create(w.psi, w.nd, w.stage, w.dtype, w.shapes, hp, units=units)
+
+
+def _timed_steps(torch, stream, step, k, flush=None):
+    """Device time of k calls of step(): one event pair around all of them, or,
+    with flush (an L2-sized write between steps), one event pair per step."""
+    if flush is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(k):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(k)]
+    for a, b in evs:
+        flush()
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs)
+
+
+def run_sweep(args):
+    """Bandwidth sweep: flat bf16 models, psi x nd, ZeRO-2, no clip (the fused
+    single pass); m and v from 5 warm-up steps; one JSON line per point."""
+    import torch
+    import gen
+    import zero_sharded_mixed_02_gb300 as z
+    from zero_sharded_mixed_02_gb300 import build as zbuild
+    from gen import workloads as W
+    zbuild.build()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    peak, _ = measured_peaks()
+    l2 = torch.empty(1 << 28, dtype=torch.uint8, device=dev)          # 256 MB > L2
+    for psi in W.SWEEP_PSI:
+        for nd in W.SWEEP_ND:
+            w = W.sweep(psi, nd)
+            line = {"mode": "sweep", "metric": "sharded Adam step HBM GB/s, bandwidth sweep",
+                    "psi": psi, "nd": nd, "zero_stage": 2, "dtype": "bf16 grads, f32 state"}
+            torch.cuda.empty_cache()
+            need = (2 * nd + 14) * psi + (1 << 30)
+            if need > torch.cuda.mem_get_info()[0]:
+                line["skipped"] = f"needs {need / 1e9:.0f} GB"
+                print(json.dumps(line), flush=True)
+                continue
+            plan = _plan_for(z, w)
+            shard, padded, _, _ = z.zero_plan_layout(plan)
+            grads = torch.empty((nd, padded), dtype=torch.int16, device=dev)
+            master = torch.zeros(padded, dtype=torch.float32, device=dev)
+            m, v = torch.zeros_like(master), torch.zeros_like(master)
+            params = torch.zeros(padded, dtype=torch.int16, device=dev)
+            gen.cuda_f32(master.data_ptr(), 0, gen.STREAM_MASTER, 0, 0, psi, 0.02, cuda_stream=sp)
+            for step in range(1, 6):                                   # 5 warm-up steps
+                gen.cuda_ranks_16(grads.data_ptr(), 0, gen.STREAM_GRAD, step, nd, psi, 1e-2, 1.0,
+                                  1, rank_stride=padded, cuda_stream=sp)
+                z.zero_step(plan, grads, master, m, v, params, None, sp)
+            gen.cuda_ranks_16(grads.data_ptr(), 0, gen.STREAM_GRAD, 6, nd, psi, 1e-2, 1.0, 1,
+                              rank_stride=padded, cuda_stream=sp)
+            small = (2 * nd + 14) * psi < (1 << 30)
+            k = max(args.steps, 200 if small else 20)
+            ms = _timed_steps(torch, stream,
+                              lambda: z.zero_step(plan, grads, master, m, v, params, None, sp),
+                              k, flush=(lambda: l2.fill_(1)) if small else None) / k
+            gbs = (2 * nd + 26) * psi / (ms / 1e3) / 1e9
+            line.update({"ms_per_step": ms, "params_per_s": psi / (ms / 1e3),
+                         "hbm_gbs_roofline_bytes": gbs, "roofline_bytes_per_elem": 2 * nd + 26,
+                         "frac_of_measured_hbm": gbs / peak, "peak_gbs": peak, "steps": k,
+                         "warmup": 5, "path": "fused single pass",
+                         "l2": "flushed between steps" if small else "inputs larger than L2"})
+            print(json.dumps(line), flush=True)
+            z.zero_plan_destroy(plan)
+            del grads, master, m, v, params
+
+
+def run_stage3(args):
+    """LLaMA-3-8B at Nd = 64, ZeRO-3: one step = the update of rank 0's resident
+    shard from its 64 contributions, then the gather of every unit (34) from the
+    64 ranks' parameter shards into one buffer."""
+    import torch
+    import gen
+    import zero_sharded_mixed_02_gb300 as z
+    from zero_sharded_mixed_02_gb300 import build as zbuild
+    zbuild.build()
+    w = workload(name="llama3-8b")
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    peak, _ = measured_peaks()
+    plan = _plan_for(z, w, units=w.units)
+    _, total, nunits, _ = z.zero_plan_layout(plan)
+    units = [z.zero_plan_unit(plan, u) for u in range(nunits)]
+    grads = torch.empty((w.nd, total), dtype=torch.int16, device=dev)
+    master = torch.zeros(total, dtype=torch.float32, device=dev)
+    m, v = torch.zeros_like(master), torch.zeros_like(master)
+    params = torch.zeros(total, dtype=torch.int16, device=dev)
+    shards = torch.empty((w.nd - 1, total), dtype=torch.int16, device=dev)
+    out = torch.empty(max(u[0] for u in units), dtype=torch.int16, device=dev)
+    gen.cuda_ranks_16(grads.data_ptr(), 0, gen.STREAM_GRAD, 1, w.nd, total, w.grad_sigma, 1.0,
+                      w.dtype, cuda_stream=sp)
+    gen.cuda_f32(master.data_ptr(), 0, gen.STREAM_MASTER, 0, 0, total, 0.02, cuda_stream=sp)
+    for k in range(1, w.nd):
+        gen.cuda_s16(shards[k - 1].data_ptr(), 0, gen.STREAM_SHARD, 0, k, total, 0.02, 1.0,
+                     w.dtype, cuda_stream=sp)
+    ptrs = [params.data_ptr()] + [shards[k].data_ptr() for k in range(w.nd - 1)]
+
+    def update():
+        z.zero_step(plan, grads, master, m, v, params, None, sp)
+
+    def gather_all():
+        for u in range(nunits):
+            z.zero_gather_layer(plan, u, ptrs, out, sp)
+
+    for _ in range(max(3, args.warmup)):
+        update()
+        gather_all()
+    torch.cuda.synchronize()
+    K = max(args.steps, 10)
+    t_upd = _timed_steps(torch, stream, update, K) / K
+    t_gat = _timed_steps(torch, stream, gather_all, K) / K
+    upd_bytes = (2 * w.nd + 26) * total
+    gat_bytes = 4 * w.psi
+    print(json.dumps({
+        "mode": "zero3", "metric": "ZeRO-3 step: resident-shard update and per-unit gathers",
+        "workload": f"{w.name}: {DESCRIPTIONS[w.name]}, {len(w.shapes)} tensors, {nunits} units",
+        "psi": w.psi, "nd": w.nd, "shard_elems": total, "steps": K,
+        "update_ms": t_upd, "update_params_per_s": total / (t_upd / 1e3),
+        "update_gbs": upd_bytes / (t_upd / 1e3) / 1e9, "update_bytes_per_elem": 2 * w.nd + 26,
+        "gather_ms_all_units": t_gat, "gather_gbs": gat_bytes / (t_gat / 1e3) / 1e9,
+        "gather_bytes_per_elem": 4, "step_ms": t_upd + t_gat,
+        "frac_of_measured_hbm": {"update": upd_bytes / (t_upd / 1e3) / 1e9 / peak,
+                                 "gather": gat_bytes / (t_gat / 1e3) / 1e9 / peak},
+        "l2": "inputs larger than L2 (16 GB gradients, 16 GB shards)"}), flush=True)
+    z.zero_plan_destroy(plan)
 
 
 # ------------------------------------------------------------ reference arm
@@ -434,7 +623,7 @@ def run_reference(args):
     rank, _, ws = dist_env()
     if rank != 0:
         return
-    w = workload(args.psi)
+    w = workload(args.psi, args.workload)
     thr = oracle_threads(w.nd)
     n_s = args.ref_sample
     import oracle
@@ -442,10 +631,10 @@ def run_reference(args):
     oracle_sample(w, n_s, thr, max_repeats=max(1, args.warmup))          # warm-up
     pps, per, reps = oracle_sample(w, n_s, thr, max_repeats=args.steps)
     out = {
-        "impl": "reference", "metric": METRIC, "value": pps, "unit": "params/s", "n_gpus": ws,
+        "impl": "reference", "metric": metric_of(w), "value": pps, "unit": "params/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic (seeded counter-based generator; GPT-2 1.5B shape list, no weights)",
+        "data": "synthetic (seeded counter-based generator; shape list only, no weights)",
         "config": config_of(w, padded),
         "cpu_baseline": {"value": pps, "unit": "params/s", "cores": thr, "kind": "oracle",
                          "sample": f"first {n_s} elements x {w.nd} ranks per step"},
@@ -463,17 +652,26 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-streams", type=int, default=1,
+                    help="copy streams the host->device gradient copy is split over")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=1 << 23)
     ap.add_argument("--ref-sample", type=int, default=1 << 21)
     ap.add_argument("--reduce-kernel", choices=("ldg", "tma"), default="ldg",
                     help="reduce-pass kernel: 128-bit loads (default) or TMA bulk staging")
+    ap.add_argument("--workload", choices=WORKLOADS, default="gpt2-1.5b")
+    ap.add_argument("--sweep", action="store_true",
+                    help="bandwidth sweep: one JSON line per (psi, nd) point")
     ap.add_argument("--psi", type=int, default=0,
                     help="flat model of this many parameters (profiling small cases)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)          # at least 3 untimed warm-up steps
     if args.impl == "reference":
         run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
+    elif args.workload == "llama3-8b":
+        run_stage3(args)
     else:
         run_ours(args)
 
