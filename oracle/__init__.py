@@ -123,6 +123,12 @@ def lib():
                 "zo_step_sharded": (ctypes.c_int, [ctypes.c_int, _I64, _I64, ctypes.c_int, _P,
                                                    _P, _P, _P, _P, _P, _P, _P, ctypes.c_int]),
                 "zo_gather_unit": (None, [ctypes.c_int, _I64, _I64, _P, _P]),
+                "zo_quantize_f32": (None, [_P, _I64, ctypes.c_int, _I64, _P, _P]),
+                "zo_dequantize_f32": (None, [_P, _P, _I64, ctypes.c_int, _I64, _P]),
+                "zo_quantize_16": (None, [ctypes.c_int, _P, _I64, ctypes.c_int, _I64, _P, _P]),
+                "zo_dequantize_16": (None, [ctypes.c_int, _P, _P, _I64, ctypes.c_int, _I64, _P]),
+                "zo_gather_unit_q": (None, [ctypes.c_int, ctypes.c_int, _I64, _I64, _I64,
+                                            ctypes.c_int, _I64, _P, _P, _P]),
                 "zo_shard_unit": (None, [ctypes.c_int, _I64, _I64, _P, _P]),
             }
             for name, (res, args) in sig.items():
@@ -246,3 +252,49 @@ def shard_unit(nd, unit, slice_elems):
     ptrs = (ctypes.c_void_p * nd)(*[_ptr(s) for s in slices])
     lib().zo_shard_unit(nd, unit.size, slice_elems, _ptr(unit), ctypes.addressof(ptrs))
     return slices
+
+
+# ---- ZeRO++ qwZ block quantization ----------------------------------------
+def code_bytes(n, bits):
+    return n if bits == 8 else (n + 1) // 2
+
+
+def quantize_f32(x, bits=8, block=256):
+    x = np.ascontiguousarray(x, np.float32)
+    q = np.zeros(code_bytes(x.size, bits), np.uint8)
+    scales = np.zeros(-(-x.size // block), np.float32)
+    lib().zo_quantize_f32(_ptr(x), x.size, bits, block, _ptr(q), _ptr(scales))
+    return q, scales
+
+
+def dequantize_f32(q, scales, n, bits=8, block=256):
+    out = np.empty(n, np.float32)
+    lib().zo_dequantize_f32(_ptr(np.ascontiguousarray(q)), _ptr(np.ascontiguousarray(scales)), n,
+                            bits, block, _ptr(out))
+    return out
+
+
+def quantize_16(dtype, x, bits=8, block=256):
+    x = np.ascontiguousarray(x, np.uint16)
+    q = np.zeros(code_bytes(x.size, bits), np.uint8)
+    scales = np.zeros(-(-x.size // block), np.float32)
+    lib().zo_quantize_16(dtype, _ptr(x), x.size, bits, block, _ptr(q), _ptr(scales))
+    return q, scales
+
+
+def dequantize_16(dtype, q, scales, n, bits=8, block=256):
+    out = np.empty(n, np.uint16)
+    lib().zo_dequantize_16(dtype, _ptr(np.ascontiguousarray(q)), _ptr(np.ascontiguousarray(scales)),
+                           n, bits, block, _ptr(out))
+    return out
+
+
+def gather_unit_q(dtype, nd, length, slice_elems, offset, bits, block, qs, scales):
+    qs = [np.ascontiguousarray(q, np.uint8) for q in qs]
+    scales = [np.ascontiguousarray(s, np.float32) for s in scales]
+    qp = (ctypes.c_void_p * nd)(*[_ptr(q) for q in qs])
+    sp = (ctypes.c_void_p * nd)(*[_ptr(s) for s in scales])
+    out = np.zeros(length, np.uint16)
+    lib().zo_gather_unit_q(dtype, nd, length, slice_elems, offset, bits, block,
+                           ctypes.addressof(qp), ctypes.addressof(sp), _ptr(out))
+    return out

@@ -411,3 +411,93 @@ void zo_shard_unit(int nd, int64_t len, int64_t slice,
             slices[k][j] = src < len ? unit[src] : (uint16_t)0;
         }
 }
+
+/* ======================================================================
+ * ZeRO++ qwZ: block-wise symmetric quantization of the weights that are
+ * gathered ([L18] 4.5).
+ * ====================================================================== */
+static int32_t round_half_even_to_int(float v)
+{
+    double r = floor((double)v);
+    double frac = (double)v - r;                       /* exact */
+    if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;
+    return (int32_t)r;
+}
+
+static void put_code(uint8_t* q, int64_t i, int bits, int32_t code)
+{
+    if (bits == 8) {
+        q[i] = (uint8_t)(int8_t)code;
+    } else {
+        uint8_t nib = (uint8_t)(code & 0xF);
+        if (i % 2 == 0) q[i / 2] = (uint8_t)((q[i / 2] & 0xF0) | nib);
+        else            q[i / 2] = (uint8_t)((q[i / 2] & 0x0F) | (nib << 4));
+    }
+}
+
+static int32_t get_code(const uint8_t* q, int64_t i, int bits)
+{
+    if (bits == 8) return (int32_t)(int8_t)q[i];
+    uint8_t nib = (i % 2 == 0) ? (q[i / 2] & 0xF) : (q[i / 2] >> 4);
+    return nib >= 8 ? (int32_t)nib - 16 : (int32_t)nib;      /* two's complement nibble */
+}
+
+void zo_quantize_f32(const float* x, int64_t n, int bits, int64_t block,
+                     uint8_t* q, float* scales)
+{
+    const float qmax = (float)((1 << (bits - 1)) - 1);
+    for (int64_t b0 = 0, blk = 0; b0 < n; b0 += block, blk++) {
+        int64_t b1 = b0 + block < n ? b0 + block : n;
+        float amax = 0.0f;
+        for (int64_t i = b0; i < b1; i++) {
+            float a = fabsf(x[i]);
+            if (a > amax) amax = a;
+        }
+        float scale = amax / qmax;
+        scales[blk] = scale;
+        for (int64_t i = b0; i < b1; i++) {
+            int32_t code = 0;
+            if (scale != 0.0f) {
+                code = round_half_even_to_int(x[i] / scale);
+                if (code > (int32_t)qmax) code = (int32_t)qmax;
+                if (code < -(int32_t)qmax) code = -(int32_t)qmax;
+            }
+            put_code(q, i, bits, code);
+        }
+    }
+}
+
+void zo_dequantize_f32(const uint8_t* q, const float* scales, int64_t n, int bits,
+                       int64_t block, float* out)
+{
+    for (int64_t i = 0; i < n; i++) out[i] = (float)get_code(q, i, bits) * scales[i / block];
+}
+
+void zo_quantize_16(int dtype, const uint16_t* x, int64_t n, int bits, int64_t block,
+                    uint8_t* q, float* scales)
+{
+    float* f = (float*)malloc((size_t)(n > 0 ? n : 1) * sizeof(float));
+    if (!f) return;
+    for (int64_t i = 0; i < n; i++) f[i] = to_float(dtype, x[i]);
+    zo_quantize_f32(f, n, bits, block, q, scales);
+    free(f);
+}
+
+void zo_dequantize_16(int dtype, const uint8_t* q, const float* scales, int64_t n, int bits,
+                      int64_t block, uint16_t* out)
+{
+    for (int64_t i = 0; i < n; i++)
+        out[i] = from_float(dtype, (float)get_code(q, i, bits) * scales[i / block]);
+}
+
+void zo_gather_unit_q(int dtype, int nd, int64_t len, int64_t slice, int64_t offset, int bits,
+                      int64_t block, const uint8_t* const* q, const float* const* scales,
+                      uint16_t* out)
+{
+    for (int64_t j = 0; j < len; j++) {
+        int64_t k = j / slice;
+        if (k >= nd) break;
+        int64_t e = offset + j % slice;             /* element of rank k's shard */
+        out[j] = from_float(dtype, (float)get_code(q[k], e, bits) * scales[k][e / block]);
+    }
+}

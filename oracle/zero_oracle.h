@@ -132,6 +132,33 @@ void zo_gather_unit(int nd, int64_t len, int64_t slice,
 void zo_shard_unit(int nd, int64_t len, int64_t slice,
                    const uint16_t* unit, uint16_t* const* slices);
 
+/* ---- ZeRO++ quantized weight gather, qwZ ([L18] 4.5: block-wise
+ *      quantization, one scale per block, so a few large values only coarsen
+ *      their own block) ------------------------------------------------------
+ * Symmetric absmax quantization to `bits` (8 or 4) bits, qmax = 2^(bits-1)-1,
+ * blocks of `block` consecutive elements (the last one may be short):
+ *   scale_b = (max_i |x_i|) / qmax                       (binary32 division)
+ *   q_i     = clamp(round_half_even(x_i / scale_b), -qmax, qmax); 0 if scale_b = 0
+ *   x'_i    = (float)q_i * scale_b                       (binary32 product)
+ * 4-bit codes are packed two per byte, element 2k in the low nibble. */
+void zo_quantize_f32(const float* x, int64_t n, int bits, int64_t block,
+                     uint8_t* q, float* scales);
+void zo_dequantize_f32(const uint8_t* q, const float* scales, int64_t n, int bits,
+                       int64_t block, float* out);
+/* The same on 16-bit values (dtype 0 fp16, 1 bf16); dequantized values are
+ * rounded to that 16-bit type. */
+void zo_quantize_16(int dtype, const uint16_t* x, int64_t n, int bits, int64_t block,
+                    uint8_t* q, float* scales);
+void zo_dequantize_16(int dtype, const uint8_t* q, const float* scales, int64_t n, int bits,
+                      int64_t block, uint16_t* out);
+/* Gather of a unit from nd quantized shards: rank k's slice of the unit starts
+ * at element `offset` of its shard; its codes and scales cover the whole shard
+ * (blocks counted from the shard's start).  out[j] for j < len is element
+ * offset + j % slice of rank j / slice's shard, dequantized. */
+void zo_gather_unit_q(int dtype, int nd, int64_t len, int64_t slice, int64_t offset, int bits,
+                      int64_t block, const uint8_t* const* q, const float* const* scales,
+                      uint16_t* out);
+
 #ifdef __cplusplus
 }
 #endif

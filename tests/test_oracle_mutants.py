@@ -12,7 +12,8 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "zero_oracle.c")
-PIN_TESTS = ["tests/test_oracle_step.py", "tests/test_oracle_formats.py"]
+PIN_TESTS = ["tests/test_oracle_step.py", "tests/test_oracle_formats.py",
+             "tests/test_oracle_quant.py"]
 
 MUTANTS = {
     "reduce-reverse-rank-order": ("for (int r = 0; r < nd; r++)\n            s = s +",
@@ -38,6 +39,13 @@ MUTANTS = {
     "round-ties-away": ("(frac == 0.5 && fmod(r, 2.0) != 0.0)", "(frac == 0.5)"),
     "gather-off-by-one": ("out[j] = slices[k][j % slice];",
                           "out[j] = slices[k][(j + 1) % slice];"),
+    "qwz-qmax-off-by-one": ("const float qmax = (float)((1 << (bits - 1)) - 1);",
+                            "const float qmax = (float)(1 << (bits - 1));"),
+    "qwz-nibble-order": ("if (i % 2 == 0) q[i / 2] = (uint8_t)((q[i / 2] & 0xF0) | nib);",
+                         "if (i % 2 == 1) q[i / 2] = (uint8_t)((q[i / 2] & 0xF0) | nib);"),
+    "qwz-truncate": ("code = round_half_even_to_int(x[i] / scale);",
+                     "code = (int32_t)(x[i] / scale);"),
+    "qwz-gather-ignores-offset": ("int64_t e = offset + j % slice;", "int64_t e = j % slice;"),
 }
 
 
