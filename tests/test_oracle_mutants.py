@@ -36,7 +36,10 @@ MUTANTS = {
     "skip-keeps-scale": ("st->loss_scale = st->loss_scale * hp->backoff;",
                          "st->loss_scale = st->loss_scale;"),
     "skip-advances-t": ("res->skipped  = 1;", "res->skipped  = 1; st->t = st->t + 1;"),
-    "round-ties-away": ("(frac == 0.5 && fmod(r, 2.0) != 0.0)", "(frac == 0.5)"),
+    "round-ties-away": ("if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;\n    return r * q;",
+                        "if (frac > 0.5 || (frac == 0.5)) r += 1.0;\n    return r * q;"),
+    "qwz-round-ties-away": ("if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;\n    return (int32_t)r;",
+                            "if (frac > 0.5 || (frac == 0.5)) r += 1.0;\n    return (int32_t)r;"),
     "gather-off-by-one": ("out[j] = slices[k][j % slice];",
                           "out[j] = slices[k][(j + 1) % slice];"),
     "qwz-qmax-off-by-one": ("const float qmax = (float)((1 << (bits - 1)) - 1);",
