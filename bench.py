@@ -602,6 +602,32 @@ def run_stage3(args):
     t_gat = _timed_steps(torch, stream, gather_all, K) / K
     upd_bytes = (2 * w.nd + 26) * total
     gat_bytes = 4 * w.psi
+    qwz = {}
+    if args.qwz:
+        bits = args.qwz
+        cbytes = total if bits == 8 else (total + 1) // 2
+        codes = torch.empty((w.nd, cbytes + 16), dtype=torch.uint8, device=dev)
+        scales = torch.empty((w.nd, -(-total // 256)), dtype=torch.float32, device=dev)
+        z.zero_quantize_shard(w.dtype, params, total, bits, codes[0], scales[0], sp)
+        for k in range(1, w.nd):
+            z.zero_quantize_shard(w.dtype, shards[k - 1], total, bits, codes[k], scales[k], sp)
+        cptr = [codes[k].data_ptr() for k in range(w.nd)]
+        sptr = [scales[k].data_ptr() for k in range(w.nd)]
+
+        def gather_all_q():
+            z.zero_quantize_shard(w.dtype, params, total, bits, codes[0], scales[0], sp)
+            for u in range(nunits):
+                z.zero_gather_layer_q(plan, u, bits, cptr, sptr, out, sp)
+
+        for _ in range(2):
+            gather_all_q()
+        t_q = _timed_steps(torch, stream, gather_all_q, K) / K
+        q_bytes = (2 + bits / 8) * total + (bits / 8 + 2) * w.psi + 4 * w.psi / 256
+        qwz = {"bits": bits, "block": 256, "quantize_and_gather_ms": t_q,
+               "bytes_per_elem": bits / 8 + 2 + 4 / 256,
+               "gbs": q_bytes / (t_q / 1e3) / 1e9,
+               "vs_unquantized_gather": t_gat / t_q,
+               "frac_of_measured_hbm": q_bytes / (t_q / 1e3) / 1e9 / peak}
     print(json.dumps({
         "mode": "zero3", "metric": "ZeRO-3 step: resident-shard update and per-unit gathers",
         "workload": f"{w.name}: {DESCRIPTIONS[w.name]}, {len(w.shapes)} tensors, {nunits} units",
@@ -612,6 +638,7 @@ def run_stage3(args):
         "gather_bytes_per_elem": 4, "step_ms": t_upd + t_gat,
         "frac_of_measured_hbm": {"update": upd_bytes / (t_upd / 1e3) / 1e9 / peak,
                                  "gather": gat_bytes / (t_gat / 1e3) / 1e9 / peak},
+        "qwz": qwz or None,
         "l2": "inputs larger than L2 (16 GB gradients, 16 GB shards)"}), flush=True)
     z.zero_plan_destroy(plan)
 
@@ -662,6 +689,8 @@ def main(argv=None):
     ap.add_argument("--workload", choices=WORKLOADS, default="gpt2-1.5b")
     ap.add_argument("--sweep", action="store_true",
                     help="bandwidth sweep: one JSON line per (psi, nd) point")
+    ap.add_argument("--qwz", type=int, choices=(0, 4, 8), default=0,
+                    help="ZeRO-3 workload: also time the quantized (qwZ) gather at this width")
     ap.add_argument("--psi", type=int, default=0,
                     help="flat model of this many parameters (profiling small cases)")
     args = ap.parse_args(argv)

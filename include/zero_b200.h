@@ -185,6 +185,31 @@ zero_status_t zero_step_overflow(zero_plan_t plan, int* overflow);
 zero_status_t zero_gather_layer(zero_plan_t plan, int unit, const void* const* shard_ptrs,
                                 void* out, void* stream);
 
+/* ---- ZeRO++ quantized weight gather (qwZ) ---------------------------------- */
+
+/* [L18] 4.5 ZeRO++: the parameters a ZeRO-3 gather moves are quantized block
+ * by block, one scale per block, so a few large weights coarsen only their own
+ * block.  A rank's 16-bit shard of n elements is cut into blocks of 256
+ * elements counted from the shard's start; for each block
+ *   scale = max|x| / qmax  (qmax = 127 for bits = 8, 7 for bits = 4; binary32)
+ *   code  = round_half_even(x / scale) clamped to [-qmax, qmax]; 0 if scale = 0.
+ * codes: n bytes (bits 8, two's complement) or ceil(n/2) bytes (bits 4, two
+ * codes per byte, the even element in the low nibble), 16-byte aligned;
+ * scales: ceil(n/256) floats.  Asynchronous.  Errors: ZERO_EINVAL, ZERO_ECUDA. */
+zero_status_t zero_quantize_shard(zero_dtype_t dtype, const void* shard, uint64_t n, int bits,
+                                  void* codes, float* scales, void* stream);
+
+/* The ZeRO-3 gather of unit `unit` from the nd ranks' quantized shards
+ * (code_ptrs[k], scale_ptrs[k]: rank k's whole-shard codes and scales, as
+ * zero_quantize_shard writes them): out[k*S_u + j] = 16-bit rounding of
+ * code_k[off_u + j] * scale_k[(off_u + j) / 256] for k*S_u + j < len.  Moves
+ * 1 (bits 8) or 0.5 (bits 4) bytes per element in instead of 2.  Errors:
+ * ZERO_EINVAL (not stage 3, unit or bits out of range, null or misaligned
+ * pointer), ZERO_ECUDA. */
+zero_status_t zero_gather_layer_q(zero_plan_t plan, int unit, int bits,
+                                  const void* const* code_ptrs, const float* const* scale_ptrs,
+                                  void* out, void* stream);
+
 /* ---- gradient norm without allocating ------------------------------------ */
 
 /* No counterpart on the pages: a convenience for callers that may not

@@ -32,7 +32,8 @@ ENTRY_POINTS = (
     "zero_plan_unit", "zero_step", "zero_step_result", "zero_step_overflow",
     "zero_gather_layer", "zero_state_bytes", "zero_comm_volume", "zero_max_params",
     "zero_status_string", "zero_plan_profile", "zero_plan_kernel_times", "zero_plan_path",
-    "zero_grad_norm_noalloc", "zero_plan_set_reduce_kernel",
+    "zero_grad_norm_noalloc", "zero_plan_set_reduce_kernel", "zero_quantize_shard",
+    "zero_gather_layer_q",
 )
 
 
@@ -99,6 +100,8 @@ def lib():
                 "zero_grad_norm_noalloc": (st, [_P, ctypes.c_int, _U64, _U64, ctypes.c_int,
                                                 ctypes.c_float, _P, _P, _P]),
                 "zero_plan_set_reduce_kernel": (st, [_P, ctypes.c_int]),
+                "zero_quantize_shard": (st, [ctypes.c_int, _P, _U64, ctypes.c_int, _P, _P, _P]),
+                "zero_gather_layer_q": (st, [_P, ctypes.c_int, ctypes.c_int, _P, _P, _P, _P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -211,6 +214,19 @@ def zero_gather_layer(plan: int, unit: int, shard_ptrs: Sequence, out, stream=0)
     arr = (ctypes.c_void_p * max(1, len(shard_ptrs)))(*[_ptr(p) for p in shard_ptrs])
     _check(lib().zero_gather_layer(plan, unit, ctypes.addressof(arr), _ptr(out), _ptr(stream)),
            "zero_gather_layer")
+
+
+def zero_quantize_shard(dtype: int, shard, n: int, bits: int, codes, scales, stream=0) -> None:
+    _check(lib().zero_quantize_shard(dtype, _ptr(shard), n, bits, _ptr(codes), _ptr(scales),
+                                     _ptr(stream)), "zero_quantize_shard")
+
+
+def zero_gather_layer_q(plan: int, unit: int, bits: int, code_ptrs: Sequence,
+                        scale_ptrs: Sequence, out, stream=0) -> None:
+    c = (ctypes.c_void_p * max(1, len(code_ptrs)))(*[_ptr(p) for p in code_ptrs])
+    s = (ctypes.c_void_p * max(1, len(scale_ptrs)))(*[_ptr(p) for p in scale_ptrs])
+    _check(lib().zero_gather_layer_q(plan, unit, bits, ctypes.addressof(c), ctypes.addressof(s),
+                                     _ptr(out), _ptr(stream)), "zero_gather_layer_q")
 
 
 def zero_state_bytes(psi: int, nd: int, stage: int, K: int = 12) -> int:

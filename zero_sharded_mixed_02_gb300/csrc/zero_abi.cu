@@ -314,6 +314,10 @@ zero_status_t fetch_mirror(zero_plan* p)
 }  // namespace
 
 namespace zero {
+int plan_nd(zero_plan_t plan) { return plan->nd; }
+int plan_stage(zero_plan_t plan) { return plan->stage; }
+int plan_dtype(zero_plan_t plan) { return (int)plan->dtype; }
+
 const void* step_kernel(int dtype, int kind, int nd)
 {
     return dtype == 0 ? step_kernel_fp16(kind, nd) : step_kernel_bf16(kind, nd);
