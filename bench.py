@@ -643,6 +643,95 @@ def run_stage3(args):
     z.zero_plan_destroy(plan)
 
 
+def run_buckets(args):
+    """Bucketed steps on the named workload: constant-size gradient buckets
+    (two buffers of nd x B 16-bit values) instead of the full nd x padded
+    gradients.  Times the bucket reduces + update alone, the synthetic backward
+    producer alone (the input generator filling each bucket, last bucket first),
+    and the two overlapped on two streams."""
+    import torch
+    import gen
+    import zero_sharded_mixed_02_gb300 as z
+    from zero_sharded_mixed_02_gb300 import build as zbuild
+    zbuild.build()
+    w = workload(args.psi, args.workload)
+    dev = torch.device("cuda", 0)
+    peak, _ = measured_peaks()
+    plan = _plan_for(z, w)
+    B = args.buckets
+    ws = z.zero_plan_set_bucket(plan, B)
+    _, padded, _, _ = z.zero_plan_layout(plan)
+    n = w.psi
+    nb = -(-n // B)
+    master = torch.zeros(padded, dtype=torch.float32, device=dev)
+    m, v = torch.zeros_like(master), torch.zeros_like(master)
+    params = torch.zeros(padded, dtype=torch.int16, device=dev)
+    work = torch.empty(ws // 4, dtype=torch.float32, device=dev)
+    bufs = [torch.empty((w.nd, B), dtype=torch.int16, device=dev) for _ in range(2)]
+    producer, consumer = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    gen.cuda_f32(master.data_ptr(), 0, gen.STREAM_MASTER, 0, 0, n, 0.02,
+                 cuda_stream=consumer.cuda_stream)
+
+    def produce(j, b, step):
+        first, count = b * B, min(B, n - b * B)
+        gen.cuda_ranks_16(bufs[j % 2].data_ptr(), 0, gen.STREAM_GRAD, step, w.nd, count,
+                          w.grad_sigma, w.loss_scale, w.dtype, rank_stride=B, index0=first,
+                          cuda_stream=producer.cuda_stream)
+
+    order = list(range(nb))[::-1]
+
+    def pipelined(step):
+        freed = [None, None]
+        for j, b in enumerate(order):
+            if freed[j % 2] is not None:
+                producer.wait_event(freed[j % 2])
+            produce(j, b, step)
+            ready = torch.cuda.Event()
+            ready.record(producer)
+            consumer.wait_event(ready)
+            z.zero_step_bucket(plan, b, bufs[j % 2], work, consumer.cuda_stream)
+            done = torch.cuda.Event()
+            done.record(consumer)
+            freed[j % 2] = done
+        z.zero_step_apply(plan, master, m, v, params, work, consumer.cuda_stream)
+
+    def reduce_only():
+        for j, b in enumerate(order):
+            z.zero_step_bucket(plan, b, bufs[j % 2], work, consumer.cuda_stream)
+        z.zero_step_apply(plan, master, m, v, params, work, consumer.cuda_stream)
+
+    def produce_only(step):
+        for j, b in enumerate(order):
+            produce(j, b, step)
+
+    def timed(fn, stream, k):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(k):
+            fn(i)
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t0) / k * 1e3
+
+    for i in range(max(3, args.warmup)):
+        pipelined(i + 1)
+    K = max(5, min(args.steps, 20))
+    t_pipe = timed(lambda i: pipelined(i + 1), consumer, K)
+    t_red = timed(lambda i: reduce_only(), consumer, K)
+    t_prod = timed(lambda i: produce_only(i + 1), producer, K)
+    step_bytes = (2 * w.nd + 26) * n
+    print(json.dumps({
+        "mode": "buckets", "metric": "bucketed step: constant-size gradient buckets",
+        "workload": f"{w.name}: {DESCRIPTIONS.get(w.name, w.name)}", "psi": n, "nd": w.nd,
+        "bucket_elems": B, "buckets": nb,
+        "gradient_staging_bytes": 2 * w.nd * B * 2, "full_gradient_bytes": w.nd * padded * 2,
+        "reduce_and_apply_ms": t_red, "producer_ms": t_prod, "pipelined_ms": t_pipe,
+        "overlap": (t_red + t_prod) / t_pipe,
+        "hbm_gbs_roofline_bytes_reduce_and_apply": step_bytes / (t_red / 1e3) / 1e9,
+        "frac_of_measured_hbm": step_bytes / (t_red / 1e3) / 1e9 / peak,
+        "timing": "host wall clock around K steps with device synchronisation"}), flush=True)
+    z.zero_plan_destroy(plan)
+
+
 # ------------------------------------------------------------ reference arm
 def run_reference(args):
     """The CPU oracle, as it stands, on the host cores: each step is one oracle
@@ -689,6 +778,8 @@ def main(argv=None):
     ap.add_argument("--workload", choices=WORKLOADS, default="gpt2-1.5b")
     ap.add_argument("--sweep", action="store_true",
                     help="bandwidth sweep: one JSON line per (psi, nd) point")
+    ap.add_argument("--buckets", type=int, default=0,
+                    help="bucketed steps with buckets of this many elements (a multiple of 64)")
     ap.add_argument("--qwz", type=int, choices=(0, 4, 8), default=0,
                     help="ZeRO-3 workload: also time the quantized (qwZ) gather at this width")
     ap.add_argument("--psi", type=int, default=0,
@@ -699,6 +790,8 @@ def main(argv=None):
         run_reference(args)
     elif args.sweep:
         run_sweep(args)
+    elif args.buckets:
+        run_buckets(args)
     elif args.workload == "llama3-8b":
         run_stage3(args)
     else:

@@ -185,6 +185,40 @@ zero_status_t zero_step_overflow(zero_plan_t plan, int* overflow);
 zero_status_t zero_gather_layer(zero_plan_t plan, int unit, const void* const* shard_ptrs,
                                 void* out, void* stream);
 
+/* ---- constant-size gradient buckets ------------------------------------------ */
+
+/* [L18] 2.3 (ZeRO-2: as soon as the backward pass has a segment's gradients they
+ * are reduced to the segment's owner and dropped, so each rank keeps only a
+ * buffer for the segment in flight; the segment reduces together are one
+ * reduce-scatter) and [L18] 4.3 / [PZ] 6.2 (a constant-size buffer worked
+ * through piece by piece instead of one flat buffer that grows with the model).
+ * A bucketed step takes the ranks' gradients bucket by bucket: bucket b covers
+ * elements [b*B, min((b+1)*B, n)) of the flat vector (stage 3: of the resident
+ * shard), B = bucket_elems (a multiple of 64).
+ *   zero_plan_set_bucket   turns bucketed steps on (B > 0) or off (B = 0) and
+ *                          reports the workspace they need: the fp32 reduced
+ *                          gradient (n floats) plus one norm partial and one
+ *                          flag per bucket.  Waits for the plan's last step.
+ *   zero_step_bucket       reduces bucket b: bucket_grads is [nd][B] 16-bit
+ *                          (rank stride B; a short last bucket uses its first
+ *                          count columns); buckets may come in any order, each
+ *                          exactly once per step (ZERO_EINVAL otherwise); the
+ *                          bucket buffer may be reused once this call's work
+ *                          on `stream` is done.
+ *   zero_step_apply        after every bucket: the global norm from the bucket
+ *                          partials (summed in bucket order), clip, skip
+ *                          decision, Adam, cast, write-back; ZERO_EINVAL if a
+ *                          bucket is missing.  zero_step_result reports it.
+ * Reduced gradients are bit-identical to zero_step's; the norm agrees to
+ * 1e-5 (its partial sums are grouped by bucket).  Calls of one plan must be
+ * ordered on one stream. */
+zero_status_t zero_plan_set_bucket(zero_plan_t plan, uint64_t bucket_elems,
+                                   uint64_t* workspace_bytes);
+zero_status_t zero_step_bucket(zero_plan_t plan, uint64_t bucket, const void* bucket_grads,
+                               void* workspace, void* stream);
+zero_status_t zero_step_apply(zero_plan_t plan, float* master, float* m, float* v, void* params,
+                              void* workspace, void* stream);
+
 /* ---- ZeRO++ quantized weight gather (qwZ) ---------------------------------- */
 
 /* [L18] 4.5 ZeRO++: the parameters a ZeRO-3 gather moves are quantized block

@@ -33,7 +33,7 @@ ENTRY_POINTS = (
     "zero_gather_layer", "zero_state_bytes", "zero_comm_volume", "zero_max_params",
     "zero_status_string", "zero_plan_profile", "zero_plan_kernel_times", "zero_plan_path",
     "zero_grad_norm_noalloc", "zero_plan_set_reduce_kernel", "zero_quantize_shard",
-    "zero_gather_layer_q",
+    "zero_gather_layer_q", "zero_plan_set_bucket", "zero_step_bucket", "zero_step_apply",
 )
 
 
@@ -102,6 +102,9 @@ def lib():
                 "zero_plan_set_reduce_kernel": (st, [_P, ctypes.c_int]),
                 "zero_quantize_shard": (st, [ctypes.c_int, _P, _U64, ctypes.c_int, _P, _P, _P]),
                 "zero_gather_layer_q": (st, [_P, ctypes.c_int, ctypes.c_int, _P, _P, _P, _P]),
+                "zero_plan_set_bucket": (st, [_P, _U64, _PU64]),
+                "zero_step_bucket": (st, [_P, _U64, _P, _P, _P]),
+                "zero_step_apply": (st, [_P, _P, _P, _P, _P, _P, _P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -214,6 +217,23 @@ def zero_gather_layer(plan: int, unit: int, shard_ptrs: Sequence, out, stream=0)
     arr = (ctypes.c_void_p * max(1, len(shard_ptrs)))(*[_ptr(p) for p in shard_ptrs])
     _check(lib().zero_gather_layer(plan, unit, ctypes.addressof(arr), _ptr(out), _ptr(stream)),
            "zero_gather_layer")
+
+
+def zero_plan_set_bucket(plan: int, bucket_elems: int) -> int:
+    """Turn bucketed steps on (bucket_elems > 0) or off; returns workspace bytes."""
+    w = ctypes.c_uint64()
+    _check(lib().zero_plan_set_bucket(plan, bucket_elems, ctypes.byref(w)), "zero_plan_set_bucket")
+    return w.value
+
+
+def zero_step_bucket(plan: int, bucket: int, bucket_grads, workspace, stream=0) -> None:
+    _check(lib().zero_step_bucket(plan, bucket, _ptr(bucket_grads), _ptr(workspace), _ptr(stream)),
+           "zero_step_bucket")
+
+
+def zero_step_apply(plan: int, master, m, v, params, workspace, stream=0) -> None:
+    _check(lib().zero_step_apply(plan, _ptr(master), _ptr(m), _ptr(v), _ptr(params),
+                                 _ptr(workspace), _ptr(stream)), "zero_step_apply")
 
 
 def zero_quantize_shard(dtype: int, shard, n: int, bits: int, codes, scales, stream=0) -> None:

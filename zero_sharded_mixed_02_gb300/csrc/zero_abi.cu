@@ -66,6 +66,12 @@ struct zero_plan {
     double ms_a = 0.0, ms_b = 0.0;
     int64_t prof_steps = 0;
     int64_t launches = 0;
+    // bucketed steps (constant-size gradient buckets)
+    uint64_t bucket_elems = 0, nbuckets = 0, bucket_ws = 0;
+    std::vector<uint8_t> bucket_seen;
+    const void* fn_bucket_reduce = nullptr;
+    const void* fn_bucket_final = nullptr;
+    const void* fn_bucket_update = nullptr;
 };
 
 namespace {
@@ -311,6 +317,28 @@ zero_status_t fetch_mirror(zero_plan* p)
     return cuda_status(e);
 }
 
+StepArgs step_args(const zero_plan* plan, const void* grads, float* master, float* m, float* v,
+                   void* params, void* workspace)
+{
+    StepArgs a;
+    a.grads = static_cast<const uint16_t*>(grads);
+    a.master = master;
+    a.m = m;
+    a.v = v;
+    a.params = static_cast<uint16_t*>(params);
+    a.g32 = static_cast<float*>(workspace);
+    a.n = (int64_t)plan->n;
+    a.rank_stride = (int64_t)plan->rank_stride;
+    a.nd = plan->nd;
+    a.k = plan->k;
+    a.clip = plan->hp.clip_norm;
+    a.dynamic = plan->hp.dynamic_scale ? 1 : 0;
+    a.backoff = plan->hp.backoff;
+    a.growth_interval = plan->hp.growth_interval;
+    a.state = plan->d_state;
+    return a;
+}
+
 }  // namespace
 
 namespace zero {
@@ -373,6 +401,117 @@ zero_status_t zero_plan_unit(zero_plan_t plan, int unit, uint64_t* len, uint64_t
 
 int zero_plan_path(zero_plan_t plan) { return plan ? plan->path : -1; }
 
+zero_status_t zero_plan_set_bucket(zero_plan_t plan, uint64_t bucket_elems,
+                                   uint64_t* workspace_bytes)
+{
+    if (!plan) return ZERO_EINVAL;
+    if (plan->stepped && cudaEventSynchronize(plan->ev_done) != cudaSuccess) return ZERO_ECUDA;
+    if (bucket_elems == 0) {
+        plan->bucket_elems = plan->nbuckets = plan->bucket_ws = 0;
+        plan->bucket_seen.clear();
+        if (workspace_bytes) *workspace_bytes = 0;
+        return ZERO_OK;
+    }
+    if (bucket_elems % LAYOUT_ALIGN != 0) return ZERO_EINVAL;
+    const uint64_t nb = ceil_div(plan->n, bucket_elems);
+    if (nb > (1ull << 24)) return ZERO_EINVAL;
+    const void* red = step_kernel((int)plan->dtype, K_REDUCE_G32, plan->nd);
+    if (!red) red = step_kernel((int)plan->dtype, K_REDUCE_G32, 0);   // generic rank count
+    const void* fin = step_kernel((int)plan->dtype, K_BUCKET_FINALIZE, 0);
+    const void* upd = step_kernel((int)plan->dtype, K_UPDATE_G32, plan->nd);
+    if (!red || !fin || !upd) return ZERO_EINVAL;
+    plan->bucket_elems = bucket_elems;
+    plan->nbuckets = nb;
+    plan->bucket_ws = round_up(plan->n * sizeof(float), 256) + round_up(nb * sizeof(double), 256) +
+                      round_up(nb * sizeof(int32_t), 256);
+    plan->bucket_seen.assign((size_t)nb, 0);
+    plan->fn_bucket_reduce = red;
+    plan->fn_bucket_final = fin;
+    plan->fn_bucket_update = upd;
+    if (workspace_bytes) *workspace_bytes = plan->bucket_ws;
+    return ZERO_OK;
+}
+
+namespace {
+void bucket_pointers(const zero_plan* plan, void* workspace, float** g32, double** partial,
+                     int32_t** flag)
+{
+    char* w = static_cast<char*>(workspace);
+    *g32 = reinterpret_cast<float*>(w);
+    w += round_up(plan->n * sizeof(float), 256);
+    *partial = reinterpret_cast<double*>(w);
+    w += round_up(plan->nbuckets * sizeof(double), 256);
+    *flag = reinterpret_cast<int32_t*>(w);
+}
+}  // namespace
+
+zero_status_t zero_step_bucket(zero_plan_t plan, uint64_t bucket, const void* bucket_grads,
+                               void* workspace, void* stream)
+{
+    if (!plan || plan->bucket_elems == 0 || bucket >= plan->nbuckets) return ZERO_EINVAL;
+    if (!bucket_grads || !aligned16(bucket_grads) || !workspace || !aligned16(workspace))
+        return ZERO_EINVAL;
+    if (plan->bucket_seen[(size_t)bucket]) return ZERO_EINVAL;        // once per step
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ZERO_ECUDA;
+    if (dev != plan->device) return ZERO_EINVAL;
+    const uint64_t first = bucket * plan->bucket_elems;
+    const uint64_t count = std::min(plan->bucket_elems, plan->n - first);
+    float* g32;
+    double* partial;
+    int32_t* flag;
+    bucket_pointers(plan, workspace, &g32, &partial, &flag);
+    StepArgs a = step_args(plan, bucket_grads, nullptr, nullptr, nullptr, nullptr, g32 + first);
+    a.n = (int64_t)count;
+    a.rank_stride = (int64_t)plan->bucket_elems;
+    a.bucket = (int)bucket;
+    a.bucket_partial = partial;
+    a.bucket_flag = flag;
+    void* args[] = {&a};
+    const int grid = grid_reduce(plan->fn_bucket_reduce, plan->sms, count, REDUCE_WAVES);
+    if (cudaLaunchKernel(plan->fn_bucket_reduce, dim3(grid), dim3(ZERO_THREADS), args, 0,
+                         static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ZERO_ECUDA;
+    plan->launches++;
+    plan->bucket_seen[(size_t)bucket] = 1;
+    return ZERO_OK;
+}
+
+zero_status_t zero_step_apply(zero_plan_t plan, float* master, float* m, float* v, void* params,
+                              void* workspace, void* stream)
+{
+    if (!plan || plan->bucket_elems == 0) return ZERO_EINVAL;
+    for (uint8_t seen : plan->bucket_seen)
+        if (!seen) return ZERO_EINVAL;                                 // a bucket is missing
+    if (plan->n > 0) {
+        const void* ptrs[] = {master, m, v, params, workspace};
+        for (const void* q : ptrs)
+            if (!q || !aligned16(q)) return ZERO_EINVAL;
+    }
+    float* g32;
+    double* partial;
+    int32_t* flag;
+    bucket_pointers(plan, workspace, &g32, &partial, &flag);
+    StepArgs a = step_args(plan, nullptr, master, m, v, params, g32);
+    a.bucket_partial = partial;
+    a.bucket_flag = flag;
+    int nb = (int)plan->nbuckets;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void* fargs[] = {&a, &nb};
+    if (cudaLaunchKernel(plan->fn_bucket_final, dim3(1), dim3(ZERO_THREADS), fargs, 0, s) !=
+        cudaSuccess)
+        return ZERO_ECUDA;
+    void* uargs[] = {&a};
+    if (cudaLaunchKernel(plan->fn_bucket_update, dim3((unsigned)plan->grid_b), dim3(ZERO_THREADS),
+                         uargs, 0, s) != cudaSuccess)
+        return ZERO_ECUDA;
+    plan->launches += 2;
+    if (cudaEventRecord(plan->ev_done, s) != cudaSuccess) return ZERO_ECUDA;
+    plan->stepped = true;
+    std::fill(plan->bucket_seen.begin(), plan->bucket_seen.end(), 0);
+    return ZERO_OK;
+}
+
 zero_status_t zero_plan_set_reduce_kernel(zero_plan_t plan, int kind)
 {
     if (!plan || (kind != 0 && kind != 1)) return ZERO_EINVAL;
@@ -426,23 +565,7 @@ zero_status_t zero_step(zero_plan_t plan, const void* grads, float* master, floa
     if (cudaGetDevice(&dev) != cudaSuccess) return ZERO_ECUDA;
     if (dev != plan->device) return ZERO_EINVAL;
 
-    StepArgs a;
-    a.grads = static_cast<const uint16_t*>(grads);
-    a.master = master;
-    a.m = m;
-    a.v = v;
-    a.params = static_cast<uint16_t*>(params);
-    a.g32 = static_cast<float*>(workspace);
-    a.n = (int64_t)plan->n;
-    a.rank_stride = (int64_t)plan->rank_stride;
-    a.nd = plan->nd;
-    a.k = plan->k;
-    a.clip = plan->hp.clip_norm;
-    a.dynamic = plan->hp.dynamic_scale ? 1 : 0;
-    a.backoff = plan->hp.backoff;
-    a.growth_interval = plan->hp.growth_interval;
-    a.state = plan->d_state;
-
+    StepArgs a = step_args(plan, grads, master, m, v, params, workspace);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     ProfileSlot* slot = nullptr;
     if (plan->profile) {

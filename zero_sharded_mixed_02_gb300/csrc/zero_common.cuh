@@ -70,6 +70,10 @@ struct StepArgs {
     float     backoff;
     int       growth_interval;
     DevState* state;
+    // bucketed step: the reduce pass covers one bucket and records its partial
+    int       bucket = -1;                // -1: a whole step
+    double*   bucket_partial = nullptr;   // [nbuckets] squared-norm partial of each bucket
+    int32_t*  bucket_flag = nullptr;      // [nbuckets] overflow flag of each bucket
 };
 
 // ---- 16-bit formats --------------------------------------------------------

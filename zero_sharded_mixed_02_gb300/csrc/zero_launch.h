@@ -13,7 +13,8 @@ enum Kind {
     K_UPDATE_G32 = 2,        // pass 2 from the fp32 gradient          (nd >= 4)
     K_UPDATE_RECOMPUTE = 3,  // pass 2 re-reading the 16-bit gradients (nd < 4)
     K_FUSED = 4,             // single pass (no clip, no dynamic scale)
-    K_REDUCE_G32_TMA = 5     // pass 1 with TMA bulk staging of the rank rows (runtime nd)
+    K_REDUCE_G32_TMA = 5,    // pass 1 with TMA bulk staging of the rank rows (runtime nd)
+    K_BUCKET_FINALIZE = 6    // bucketed step: norm and bookkeeping from the bucket partials
 };
 
 // Kernel function for (dtype, kind, nd); nullptr if that combination is not

@@ -104,9 +104,32 @@ static __device__ __forceinline__ void reduce_and_finalize(const StepArgs& a, do
     const double total = block_sum(x, sh.d);
     const int    any   = block_or(f, sh.i);
     if (threadIdx.x == 0) {
-        finalize(a, total, any);
+        if (a.bucket >= 0) {                       // one bucket of a bucketed step
+            a.bucket_partial[a.bucket] = total;
+            a.bucket_flag[a.bucket] = any;
+        } else {
+            finalize(a, total, any);
+        }
         a.state->counter = 0;
     }
+}
+
+// Bucketed step, after every bucket is reduced: the global norm and overflow flag
+// from the bucket partials, combined in bucket order by one block, then the
+// step's scalar bookkeeping.
+template <int DT>
+__global__ void __launch_bounds__(ZERO_THREADS) k_bucket_finalize(const StepArgs a, int nbuckets)
+{
+    __shared__ RedShared sh;
+    double x = 0.0;
+    int f = 0;
+    for (int b = threadIdx.x; b < nbuckets; b += blockDim.x) {
+        x += a.bucket_partial[b];
+        f |= a.bucket_flag[b];
+    }
+    const double total = block_sum(x, sh.d);
+    const int any = block_or(f, sh.i);
+    if (threadIdx.x == 0) finalize(a, total, any);
 }
 
 static __device__ __forceinline__ void unpack8(const float4 a, const float4 b, float (&x)[8])

@@ -32,6 +32,7 @@ static const void* fused_or_reduce(int kind)
 template <int DT>
 static const void* step_kernel_dt(int kind, int nd)
 {
+    if (kind == K_BUCKET_FINALIZE) return (const void*)k_bucket_finalize<DT>;
     if (kind == K_REDUCE_G32_TMA) {
         switch (nd) {
         case 4:  return (const void*)k_reduce_tma<DT, 4>;
