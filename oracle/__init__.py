@@ -130,6 +130,9 @@ def lib():
                 "zo_gather_unit_q": (None, [ctypes.c_int, ctypes.c_int, _I64, _I64, _I64,
                                             ctypes.c_int, _I64, _P, _P, _P]),
                 "zo_shard_unit": (None, [ctypes.c_int, _I64, _I64, _P, _P]),
+                "zo_layout_shard_len": (_I64, [_P]),
+                "zo_layout_global": (_I64, [_P, ctypes.c_int, _I64]),
+                "zo_reshard": (None, [_P, _P, _P, _P, ctypes.c_int]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -252,6 +255,45 @@ def shard_unit(nd, unit, slice_elems):
     ptrs = (ctypes.c_void_p * nd)(*[_ptr(s) for s in slices])
     lib().zo_shard_unit(nd, unit.size, slice_elems, _ptr(unit), ctypes.addressof(ptrs))
     return slices
+
+
+# ---- sharded checkpoint: regrouping shards for another layout ---------------
+class _Layout(ctypes.Structure):
+    _fields_ = [("nd", ctypes.c_int), ("nunits", ctypes.c_int), ("len", ctypes.c_void_p)]
+
+
+class Layout:
+    """nd ranks over units of the given lengths (stages 0-2: one unit of psi)."""
+
+    def __init__(self, nd, unit_lens):
+        self.nd = int(nd)
+        self.lens = np.ascontiguousarray(np.asarray(unit_lens, dtype=np.int64))
+        self.c = _Layout(self.nd, int(self.lens.size), _ptr(self.lens))
+
+    @property
+    def psi(self):
+        return int(self.lens.sum())
+
+    def shard_len(self):
+        return int(lib().zo_layout_shard_len(ctypes.byref(self.c)))
+
+    def global_index(self, r, j):
+        return int(lib().zo_layout_global(ctypes.byref(self.c), r, j))
+
+
+def reshard(A, old_shards, B):
+    """old_shards: A.nd arrays of A.shard_len() elements (one dtype) -> B.nd arrays."""
+    old = [np.ascontiguousarray(x) for x in old_shards]
+    dt = old[0].dtype
+    assert all(x.dtype == dt and x.size == A.shard_len() for x in old) and len(old) == A.nd
+    new = [np.empty(B.shard_len(), dt) for _ in range(B.nd)]
+    for x in new:                                   # nonzero fill: padding must be written
+        x.view(np.uint8)[:] = 0xA5
+    po = (ctypes.c_void_p * A.nd)(*[_ptr(x) for x in old])
+    pn = (ctypes.c_void_p * B.nd)(*[_ptr(x) for x in new])
+    lib().zo_reshard(ctypes.byref(A.c), ctypes.addressof(po), ctypes.byref(B.c),
+                     ctypes.addressof(pn), dt.itemsize)
+    return new
 
 
 # ---- ZeRO++ qwZ block quantization ----------------------------------------

@@ -501,3 +501,58 @@ void zo_gather_unit_q(int dtype, int nd, int64_t len, int64_t slice, int64_t off
         out[j] = from_float(dtype, (float)get_code(q[k], e, bits) * scales[k][e / block]);
     }
 }
+
+/* ======================================================================
+ * Sharded checkpoint: regroup the shards of one layout into another
+ * ([Z026] sec. 5; [L32] sec. 4.3).  Written as the definition: every shard
+ * position names one flat index (or padding); the flat vector is rebuilt from
+ * the old layout and read back through the new one.
+ * ====================================================================== */
+int64_t zo_layout_shard_len(const zo_layout* L)
+{
+    int64_t total = 0;
+    for (int u = 0; u < L->nunits; u++) total += zo_shard_elems(L->len[u], L->nd);
+    return total;
+}
+
+int64_t zo_layout_global(const zo_layout* L, int r, int64_t j)
+{
+    int64_t unit_start = 0;                   /* flat index of the unit's first element */
+    int64_t slice_start = 0;                  /* shard position of the unit's slice     */
+    for (int u = 0; u < L->nunits; u++) {
+        int64_t s = zo_shard_elems(L->len[u], L->nd);
+        if (j < slice_start + s) {
+            int64_t local = (int64_t)r * s + (j - slice_start);   /* element of the unit */
+            return local < L->len[u] ? unit_start + local : -1;
+        }
+        unit_start += L->len[u];
+        slice_start += s;
+    }
+    return -1;
+}
+
+void zo_reshard(const zo_layout* A, const void* const* old_shards, const zo_layout* B,
+                void* const* new_shards, int elem_bytes)
+{
+    int64_t psi = 0;
+    for (int u = 0; u < A->nunits; u++) psi += A->len[u];
+    unsigned char* flat = (unsigned char*)calloc((size_t)(psi > 0 ? psi : 1), (size_t)elem_bytes);
+    if (!flat) return;
+    int64_t la = zo_layout_shard_len(A);
+    for (int r = 0; r < A->nd; r++)
+        for (int64_t j = 0; j < la; j++) {
+            int64_t g = zo_layout_global(A, r, j);
+            if (g >= 0)
+                memcpy(flat + g * elem_bytes,
+                       (const unsigned char*)old_shards[r] + j * elem_bytes, (size_t)elem_bytes);
+        }
+    int64_t lb = zo_layout_shard_len(B);
+    for (int r = 0; r < B->nd; r++)
+        for (int64_t j = 0; j < lb; j++) {
+            int64_t g = zo_layout_global(B, r, j);
+            unsigned char* dst = (unsigned char*)new_shards[r] + j * elem_bytes;
+            if (g >= 0) memcpy(dst, flat + g * elem_bytes, (size_t)elem_bytes);
+            else memset(dst, 0, (size_t)elem_bytes);
+        }
+    free(flat);
+}

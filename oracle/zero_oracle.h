@@ -159,6 +159,33 @@ void zo_gather_unit_q(int dtype, int nd, int64_t len, int64_t slice, int64_t off
                       int64_t block, const uint8_t* const* q, const float* const* scales,
                       uint16_t* out);
 
+/* ---- sharded checkpoint: ownership regrouped for another rank count
+ *      ([Z026] sec. 5: restoring at a different degree of parallelism must
+ *      reorganise which rank owns what while keeping the parameter order and
+ *      each element's moments together; [L32] sec. 4.3: the checkpoint holds
+ *      the sharded optimizer state) --------------------------------------------
+ * A layout of psi flat elements over nd ranks: nunits units of len[u]
+ * consecutive flat elements (stages 0-2: one unit, len[0] = psi; stage 3: the
+ * ZeRO-3 units in order).  Unit u is cut into nd slices of
+ * S_u = zo_shard_elems(len[u], nd) elements; rank r's shard is the
+ * concatenation, in unit order, of element r*S_u .. (r+1)*S_u - 1 of every
+ * unit (positions past len[u] are padding). */
+typedef struct {
+    int nd;
+    int nunits;
+    const int64_t* len;
+} zo_layout;
+
+/* elements of one rank's shard: the sum of the S_u */
+int64_t zo_layout_shard_len(const zo_layout* L);
+/* flat index held at position j of rank r's shard; -1 for padding */
+int64_t zo_layout_global(const zo_layout* L, int r, int64_t j);
+/* Regroup: old_shards[r] (layout A, elem_bytes-wide elements) -> new_shards[r]
+ * (layout B): each position of B takes the element of A that holds the same
+ * flat index; padding positions of B are zero.  Both layouts cover the same psi. */
+void zo_reshard(const zo_layout* A, const void* const* old_shards, const zo_layout* B,
+                void* const* new_shards, int elem_bytes);
+
 #ifdef __cplusplus
 }
 #endif

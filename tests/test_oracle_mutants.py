@@ -13,7 +13,7 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "zero_oracle.c")
 PIN_TESTS = ["tests/test_oracle_step.py", "tests/test_oracle_formats.py",
-             "tests/test_oracle_quant.py"]
+             "tests/test_oracle_quant.py", "tests/test_oracle_ckpt.py"]
 
 MUTANTS = {
     "reduce-reverse-rank-order": ("for (int r = 0; r < nd; r++)\n            s = s +",
@@ -49,6 +49,14 @@ MUTANTS = {
     "qwz-truncate": ("code = round_half_even_to_int(x[i] / scale);",
                      "code = (int32_t)(x[i] / scale);"),
     "qwz-gather-ignores-offset": ("int64_t e = offset + j % slice;", "int64_t e = j % slice;"),
+    "reshard-padding-kept": ("else memset(dst, 0, (size_t)elem_bytes);", "else { }"),
+    "layout-slice-start-dropped": ("int64_t local = (int64_t)r * s + (j - slice_start);",
+                                   "int64_t local = (int64_t)r * s + j;"),
+    "layout-unit-start-dropped": ("return local < L->len[u] ? unit_start + local : -1;",
+                                  "return local < L->len[u] ? local : -1;"),
+    "layout-boundary-off-by-one": ("if (j < slice_start + s) {", "if (j <= slice_start + s) {"),
+    "reshard-ranks-reversed": ("int64_t g = zo_layout_global(A, r, j);",
+                               "int64_t g = zo_layout_global(A, A->nd - 1 - r, j);"),
 }
 
 
