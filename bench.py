@@ -732,6 +732,113 @@ def run_buckets(args):
     z.zero_plan_destroy(plan)
 
 
+def run_checkpoint(args):
+    """Sharded checkpoint of the workload's optimizer state through the C ABI:
+    every rank's file saved (into the page cache, then flushed to storage with
+    the files' cached pages dropped), then loaded into a plan at half the rank
+    count (a reshard) from storage and again from the page cache.  Wall-clock
+    times of the synchronous calls; loaded state checked on sampled elements."""
+    import dataclasses
+    import shutil
+    import tempfile
+    import torch
+    import gen
+    import zero_sharded_mixed_02_gb300 as z
+    from zero_sharded_mixed_02_gb300 import build as zbuild
+    zbuild.build()
+    w = workload(args.psi, args.workload)
+    if w.stage == 3:
+        print(json.dumps({"mode": "checkpoint", "workload": w.name,
+                          "unavailable": "a ZeRO-3 plan holds one rank's shard; this mode "
+                                         "saves every rank of a stages 0-2 plan"}), flush=True)
+        return
+    dev = torch.device("cuda", 0)
+    state_bytes = 14 * w.psi                      # master, m, v (fp32) + 16-bit params
+    base = args.ckpt_dir or tempfile.gettempdir()
+    free = shutil.disk_usage(base).free
+    line = {"mode": "checkpoint", "workload": f"{w.name}: {DESCRIPTIONS.get(w.name, w.name)}",
+            "psi": w.psi, "nd_saved": w.nd, "nd_loaded": max(1, w.nd // 2),
+            "checkpoint_bytes": state_bytes, "dir_free_bytes": free}
+    if free < 2.5 * state_bytes:
+        line["unavailable"] = f"{base} has {free} bytes free; needs {int(2.5 * state_bytes)}"
+        print(json.dumps(line), flush=True)
+        return
+    d = tempfile.mkdtemp(prefix="zck_", dir=base)
+    plan = _plan_for(z, w)
+    w2 = dataclasses.replace(w, nd=max(1, w.nd // 2))
+    plan2 = _plan_for(z, w2)
+    try:
+        _, padded, _, _ = z.zero_plan_layout(plan)
+        _, padded2, _, _ = z.zero_plan_layout(plan2)
+        a = [torch.zeros(padded, dtype=torch.float32, device=dev) for _ in range(3)]
+        a.append(torch.zeros(padded, dtype=torch.int16, device=dev))
+        gen.cuda_f32(a[0].data_ptr(), 0, gen.STREAM_MASTER, 0, 0, w.psi, 0.02)
+        a[1][:w.psi].normal_()
+        a[2][:w.psi].uniform_()
+        a[3][:w.psi].random_(-32768, 32767)
+        b = [torch.full((padded2,), 3.0, dtype=torch.float32, device=dev) for _ in range(3)]
+        b.append(torch.full((padded2,), 7, dtype=torch.int16, device=dev))
+        torch.cuda.synchronize()
+
+        def clock(fn):
+            t0 = time.perf_counter()
+            fn()
+            return time.perf_counter() - t0
+
+        t = {}
+        flags = z.ZERO_CKPT_FSYNC | z.ZERO_CKPT_DROP_CACHE
+        t["save_fsync"] = clock(lambda: z.zero_checkpoint_save(plan, d + "/s", -1, *a, flags))
+        t["load_after_drop"] = clock(lambda: z.zero_checkpoint_load(plan2, d + "/s", -1, *b))
+        t["load_page_cache"] = clock(lambda: z.zero_checkpoint_load(plan2, d + "/s", -1, *b))
+        idx = torch.randint(0, w.psi, (1 << 20,), device=dev)
+        ok = all(torch.equal(x[idx], y[idx]) for x, y in zip(a, b))
+        ok = ok and not any(bool(y[w.psi:].any()) for y in b)
+        os.sync()
+        t["save_page_cache"] = clock(lambda: z.zero_checkpoint_save(plan, d + "/c", -1, *a))
+        shutil.rmtree(d + "/c")
+        os.sync()
+        # the device<->host link, for scale: one pinned copy each way
+        nl = min(1 << 28, padded)
+        host = torch.empty(nl, dtype=torch.float32, pin_memory=True)
+        src = a[0][:nl]
+        for _ in range(2):
+            host.copy_(src, non_blocking=True)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        host.copy_(src, non_blocking=True)
+        torch.cuda.synchronize()
+        d2h = nl * 4 / (time.perf_counter() - t0) / 1e9
+        t0 = time.perf_counter()
+        src.copy_(host, non_blocking=True)
+        torch.cuda.synchronize()
+        h2d = nl * 4 / (time.perf_counter() - t0) / 1e9
+        # the storage under `base`, for scale: dd of 4 GiB, flushed / read direct
+        dd = {}
+        ddf = d + "/dd.bin"
+        try:
+            t0 = time.perf_counter()
+            subprocess.run(["dd", "if=/dev/zero", f"of={ddf}", "bs=64M", "count=64",
+                            "conv=fsync"], check=True, capture_output=True)
+            dd["dd_write_fsync_gbs"] = (64 << 26) / (time.perf_counter() - t0) / 1e9
+            t0 = time.perf_counter()
+            subprocess.run(["dd", f"if={ddf}", "of=/dev/null", "bs=64M", "iflag=direct"],
+                           check=True, capture_output=True)
+            dd["dd_read_direct_gbs"] = (64 << 26) / (time.perf_counter() - t0) / 1e9
+        except (OSError, subprocess.CalledProcessError) as e:
+            dd["dd"] = f"not measured: {e}"
+        line.update({f"{k}_s": v for k, v in t.items()})
+        line.update({f"{k}_gbs": state_bytes / v / 1e9 for k, v in t.items()})
+        line.update(dd)
+        line.update({"link_d2h_gbs": d2h, "link_h2d_gbs": h2d, "verified_sample": bool(ok),
+                     "host_threads": os.cpu_count(), "dir": base,
+                     "timing": "host wall clock around each synchronous call"})
+        print(json.dumps(line), flush=True)
+    finally:
+        z.zero_plan_destroy(plan)
+        z.zero_plan_destroy(plan2)
+        shutil.rmtree(d, ignore_errors=True)
+
+
 # ------------------------------------------------------------ reference arm
 def run_reference(args):
     """The CPU oracle, as it stands, on the host cores: each step is one oracle
@@ -778,6 +885,9 @@ def main(argv=None):
     ap.add_argument("--workload", choices=WORKLOADS, default="gpt2-1.5b")
     ap.add_argument("--sweep", action="store_true",
                     help="bandwidth sweep: one JSON line per (psi, nd) point")
+    ap.add_argument("--checkpoint", action="store_true",
+                    help="time a sharded checkpoint save and a resharding load of the workload")
+    ap.add_argument("--ckpt-dir", default=None, help="where --checkpoint writes (default: tmp)")
     ap.add_argument("--buckets", type=int, default=0,
                     help="bucketed steps with buckets of this many elements (a multiple of 64)")
     ap.add_argument("--qwz", type=int, choices=(0, 4, 8), default=0,
@@ -792,6 +902,8 @@ def main(argv=None):
         run_sweep(args)
     elif args.buckets:
         run_buckets(args)
+    elif args.checkpoint:
+        run_checkpoint(args)
     elif args.workload == "llama3-8b":
         run_stage3(args)
     else:

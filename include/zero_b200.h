@@ -57,7 +57,13 @@ typedef enum {
     ZERO_EINVAL   = 1,   /* an argument is out of range, null or misaligned   */
     ZERO_ENOMEM   = 2,   /* host or device allocation failed                  */
     ZERO_ECUDA    = 3,   /* a CUDA call or kernel launch failed                */
-    ZERO_ETIMEOUT = 4    /* a bounded device-side wait gave up                 */
+    ZERO_ETIMEOUT = 4,   /* a bounded device-side wait gave up                 */
+    ZERO_ENOENT   = 5,   /* a checkpoint file is missing or cannot be opened   */
+    ZERO_ECORRUPT = 6,   /* a checkpoint file is truncated, fails a checksum,
+                            or does not belong with the other files           */
+    ZERO_EIO      = 7,   /* reading, writing or flushing a file failed         */
+    ZERO_ESTATE   = 8    /* a failed checkpoint load left the plan's state
+                            incomplete; steps are refused until a load succeeds */
 } zero_status_t;
 
 typedef enum { ZERO_FP16 = 0, ZERO_BF16 = 1 } zero_dtype_t;
@@ -272,6 +278,88 @@ zero_status_t zero_gather_layer_q(zero_plan_t plan, int unit, int bits,
 zero_status_t zero_grad_norm_noalloc(const void* grads, int nd, uint64_t n, uint64_t rank_stride,
                                      zero_dtype_t dtype, float loss_scale, double* norm_out,
                                      int* overflow_out, void* stream);
+
+/* ---- sharded checkpoint ------------------------------------------------------ */
+/* [Z026] sec. 5: with the state sharded, each rank holds only its part of the
+ * weights and optimizer state; a restore at another degree of parallelism
+ * must regroup ownership while keeping the parameter order and each
+ * element's moments together, and a rank's missing file must make the
+ * restore fail explicitly rather than produce an incomplete model.
+ * [L32] sec. 4.3: a resumable checkpoint holds the sharded optimizer state,
+ * not the weights alone.
+ *
+ * A checkpoint is a directory holding manifest.zck and one file per rank of
+ * the saving plan, shard_<rank>_of_<nd>.zck (5-digit decimal, zero-padded).
+ * Each rank file holds, for the flat elements that rank owns (padding
+ * excluded): master, m and v (fp32) and the 16-bit parameters.  The file
+ * records those elements as segments [global_start, global_start + count) of
+ * the flat parameter vector, so a checkpoint does not depend on the saving
+ * plan's rank count or stage: a plan of any nd and stage over the same tensor
+ * list can load it, each of its ranks taking the elements it owns.
+ *
+ * Format (all integers little-endian):
+ *   manifest.zck, 88 bytes: "ZEROMAN1", u32 version (1), u32 size (88),
+ *     u64 psi, i32 nd, i32 stage, i32 dtype, i32 0, u64 model_hash,
+ *     scalars (32 bytes: f32 loss_scale, i32 good_steps, i64 t, f64 beta1^t,
+ *     f64 beta2^t), u64 zck64 of bytes 0..79.
+ *   shard file: a 4096-byte header: "ZEROSHD1", u32 version (1),
+ *     u32 4096, u64 psi, i32 nd, i32 stage, i32 dtype, i32 rank,
+ *     u64 model_hash, scalars (32 bytes, as above), u64 nseg, u64 n (elements
+ *     held = sum of the segment counts), u64 block_elems (2^20), u64 nblocks
+ *     (ceil(n / block_elems)), u64 table_offset (4096), u64 array_offset[4]
+ *     (master, m, v, params), u64 file_bytes, u64 meta_hash; zeros up to 4096.
+ *     At table_offset: nseg pairs {u64 global_start, u64 count} in shard
+ *     order, then 4 x nblocks u64 block checksums (array a, block b at
+ *     a * nblocks + b).  Each array holds its n values in segment order and
+ *     starts on a 4096-byte boundary.  meta_hash = zck64 of header bytes
+ *     0..159 plus zck64 of the table, mod 2^64.
+ *   zck64 of a byte string whose first 8-byte word has index w0 within its
+ *     array: the sum mod 2^64, over its 8-byte words x_i (the last one
+ *     zero-padded), of mix(x_i + (w0 + i + 1) * 0x9E3779B97F4A7C15), where
+ *     mix is the SplitMix64 finaliser (z ^= z >> 30; z *= 0xBF58476D1CE4E5B9;
+ *     z ^= z >> 27; z *= 0x94D049BB133111EB; z ^= z >> 31).  Block b of an
+ *     array covers elements [b * 2^20, min((b + 1) * 2^20, n)), w0 = its byte
+ *     offset / 8.
+ *   model_hash: FNV-1a 64 over the little-endian bytes of the int64 values
+ *     ntensors, then for each tensor its ndims and its dims.
+ */
+
+/* flags of zero_checkpoint_save */
+#define ZERO_CKPT_FSYNC      1   /* flush every file and the directory to storage  */
+#define ZERO_CKPT_DROP_CACHE 2   /* with FSYNC: then drop the files' cached pages  */
+
+/* Save rank `rank`'s state, or every rank's (rank = -1; stages 0-2 only).
+ * Buffers: as zero_step.  Stages 0-2: the flat [nd*S] master, m, v, params;
+ * stage 3: rank `rank`'s resident shard.  Writes shard_<rank>_of_<nd>.zck
+ * (through a temporary name, renamed when complete) for each rank saved, and
+ * manifest.zck when rank is 0 or -1, creating `dir` if it does not exist.
+ * The scalars (loss scale, good steps, t, beta powers) are the plan's after
+ * its last step.  Synchronous: waits for `stream` and the plan's last step,
+ * returns when the files are written.  Host staging is pinned memory the plan
+ * keeps until it is destroyed.
+ * Errors: ZERO_EINVAL (null, misaligned or out-of-range argument), ZERO_EIO
+ * (a file could not be created, written or flushed; no partial file is left
+ * under the final name), ZERO_ENOMEM, ZERO_ECUDA. */
+zero_status_t zero_checkpoint_save(zero_plan_t plan, const char* dir, int rank,
+                                   const float* master, const float* m, const float* v,
+                                   const void* params, int flags, void* stream);
+
+/* Load rank `rank`'s state, or every rank's (rank = -1; stages 0-2 only), from
+ * the checkpoint in `dir`, whatever rank count and stage saved it; the
+ * elements of the plan's layout past each unit's or the model's end are set
+ * to zero.  Buffers: as zero_checkpoint_save.  On success the plan's scalars
+ * are the checkpoint's and its last-step report is reset.  Synchronous.
+ * Checks, before any device memory is written: the manifest and every one of
+ * the saving plan's rank files exist (ZERO_ENOENT), their headers are intact
+ * and agree with each other, their segments cover the flat vector exactly once
+ * (ZERO_ECORRUPT), and the model is the plan's: same psi, tensor shape list
+ * and 16-bit type (ZERO_EINVAL); the buffers are then untouched.  Every data
+ * block read is checked against its checksum; a mismatch or read error after
+ * device writes began returns ZERO_ECORRUPT or ZERO_EIO and leaves the plan
+ * refusing steps and gathers (ZERO_ESTATE) until a load succeeds.
+ * Other errors: ZERO_ENOMEM, ZERO_ECUDA. */
+zero_status_t zero_checkpoint_load(zero_plan_t plan, const char* dir, int rank, float* master,
+                                   float* m, float* v, void* params, void* stream);
 
 /* ---- memory ledger and communication volume ------------------------------- */
 

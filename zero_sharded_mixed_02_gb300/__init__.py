@@ -22,7 +22,9 @@ from typing import Optional, Sequence, Tuple
 _DIR = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_DIR, "libzero_b200.so")
 
-ZERO_OK, ZERO_EINVAL, ZERO_ENOMEM, ZERO_ECUDA, ZERO_ETIMEOUT = range(5)
+(ZERO_OK, ZERO_EINVAL, ZERO_ENOMEM, ZERO_ECUDA, ZERO_ETIMEOUT, ZERO_ENOENT, ZERO_ECORRUPT,
+ ZERO_EIO, ZERO_ESTATE) = range(9)
+ZERO_CKPT_FSYNC, ZERO_CKPT_DROP_CACHE = 1, 2
 ZERO_FP16, ZERO_BF16 = 0, 1
 PATH_FUSED, PATH_G32, PATH_RECOMPUTE = 0, 1, 2
 
@@ -34,6 +36,7 @@ ENTRY_POINTS = (
     "zero_status_string", "zero_plan_profile", "zero_plan_kernel_times", "zero_plan_path",
     "zero_grad_norm_noalloc", "zero_plan_set_reduce_kernel", "zero_quantize_shard",
     "zero_gather_layer_q", "zero_plan_set_bucket", "zero_step_bucket", "zero_step_apply",
+    "zero_checkpoint_save", "zero_checkpoint_load",
 )
 
 
@@ -105,6 +108,10 @@ def lib():
                 "zero_plan_set_bucket": (st, [_P, _U64, _PU64]),
                 "zero_step_bucket": (st, [_P, _U64, _P, _P, _P]),
                 "zero_step_apply": (st, [_P, _P, _P, _P, _P, _P, _P]),
+                "zero_checkpoint_save": (st, [_P, ctypes.c_char_p, ctypes.c_int, _P, _P, _P, _P,
+                                              ctypes.c_int, _P]),
+                "zero_checkpoint_load": (st, [_P, ctypes.c_char_p, ctypes.c_int, _P, _P, _P, _P,
+                                              _P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -234,6 +241,22 @@ def zero_step_bucket(plan: int, bucket: int, bucket_grads, workspace, stream=0) 
 def zero_step_apply(plan: int, master, m, v, params, workspace, stream=0) -> None:
     _check(lib().zero_step_apply(plan, _ptr(master), _ptr(m), _ptr(v), _ptr(params),
                                  _ptr(workspace), _ptr(stream)), "zero_step_apply")
+
+
+def zero_checkpoint_save(plan: int, directory: str, rank: int, master, m, v, params,
+                         flags: int = 0, stream=0) -> None:
+    """rank -1: every rank (stages 0-2).  Synchronous."""
+    _check(lib().zero_checkpoint_save(plan, os.fsencode(directory), rank, _ptr(master), _ptr(m),
+                                      _ptr(v), _ptr(params), flags, _ptr(stream)),
+           "zero_checkpoint_save")
+
+
+def zero_checkpoint_load(plan: int, directory: str, rank: int, master, m, v, params,
+                         stream=0) -> None:
+    """rank -1: every rank (stages 0-2).  Synchronous."""
+    _check(lib().zero_checkpoint_load(plan, os.fsencode(directory), rank, _ptr(master), _ptr(m),
+                                      _ptr(v), _ptr(params), _ptr(stream)),
+           "zero_checkpoint_load")
 
 
 def zero_quantize_shard(dtype: int, shard, n: int, bits: int, codes, scales, stream=0) -> None:

@@ -18,7 +18,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libzero_b200.so")
 
 SOURCES = ["zero_abi.cu", "zero_step_fp16.cu", "zero_step_bf16.cu", "zero_gather.cu",
-           "zero_noalloc.cu", "zero_qwz.cu"]
+           "zero_noalloc.cu", "zero_qwz.cu", "zero_ckpt.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                      "-I", INCLUDE, "-I", CSRC]
@@ -64,7 +64,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if failed:
         raise RuntimeError("nvcc failed:\n" + "\n".join(failed))
     tmp = LIB + f".tmp{os.getpid()}"
-    subprocess.run(["nvcc", *ARCH, "-shared", "-o", tmp, *objs], check=True)
+    subprocess.run(["nvcc", *ARCH, "-shared", "-o", tmp, *objs, "-lpthread"], check=True)
     os.replace(tmp, LIB)
     return LIB
 

@@ -9,6 +9,7 @@
 
 #include "zero_b200.h"
 #include "zero_launch.h"
+#include "zero_plan_access.h"
 
 using namespace zero;
 
@@ -72,6 +73,11 @@ struct zero_plan {
     const void* fn_bucket_reduce = nullptr;
     const void* fn_bucket_final = nullptr;
     const void* fn_bucket_update = nullptr;
+    // checkpoints
+    uint64_t model_hash = 0;          // FNV-1a 64 of the tensor shape list
+    bool poisoned = false;            // a failed load left the state half-written
+    std::vector<void*> staging;       // pinned host staging for checkpoint IO
+    uint64_t staging_bytes = 0;
 };
 
 namespace {
@@ -110,6 +116,7 @@ void destroy_plan(zero_plan* p)
     if (p->h_mirror) cudaFreeHost(p->h_mirror);
     if (p->ev_done) cudaEventDestroy(p->ev_done);
     if (p->copy_stream) cudaStreamDestroy(p->copy_stream);
+    for (void* b : p->staging) cudaFreeHost(b);
     delete p;
 }
 
@@ -132,6 +139,27 @@ int grid_reduce(const void* fn, int sms, uint64_t n, uint64_t waves)
 uint64_t grid_update(uint64_t n)
 {
     return std::max<uint64_t>(1, ceil_div(ceil_div(n, 4), ZERO_THREADS));
+}
+
+// FNV-1a 64 over the little-endian bytes of the int64 sequence ntensors,
+// then for each tensor its ndims and its dims: the identity of a model's
+// parameter list, stored in checkpoints.
+uint64_t shape_hash(const int64_t* dims, const int* ndims, int ntensors)
+{
+    uint64_t h = 0xCBF29CE484222325ull;
+    auto put = [&h](int64_t x) {
+        for (int b = 0; b < 8; b++) {
+            h ^= (uint64_t)((uint64_t)x >> (8 * b)) & 0xFFu;
+            h *= 0x100000001B3ull;
+        }
+    };
+    put(ntensors);
+    size_t di = 0;
+    for (int t = 0; t < ntensors; t++) {
+        put(ndims[t]);
+        for (int d = 0; d < ndims[t]; d++) put(dims[di++]);
+    }
+    return h;
 }
 
 zero_status_t create_impl(uint64_t psi, int nd, int stage, zero_dtype_t dtype,
@@ -167,6 +195,7 @@ zero_status_t create_impl(uint64_t psi, int nd, int stage, zero_dtype_t dtype,
 
     zero_plan* p = new (std::nothrow) zero_plan();
     if (!p) return ZERO_ENOMEM;
+    p->model_hash = shape_hash(dims, ndims, ntensors);
     p->psi = psi;
     p->nd = nd;
     p->stage = stage;
@@ -346,6 +375,82 @@ int plan_nd(zero_plan_t plan) { return plan->nd; }
 int plan_stage(zero_plan_t plan) { return plan->stage; }
 int plan_dtype(zero_plan_t plan) { return (int)plan->dtype; }
 
+void plan_layout(zero_plan_t plan, PlanLayout* out)
+{
+    out->psi = plan->psi;
+    out->nd = plan->nd;
+    out->stage = plan->stage;
+    out->dtype = (int)plan->dtype;
+    out->device = plan->device;
+    out->shard = plan->stage <= 2 ? plan->shard : plan->shard_total;
+    out->model_hash = plan->model_hash;
+    out->unit_len = plan->unit_len;
+    out->unit_slice = plan->unit_slice;
+    out->unit_off = plan->unit_off;
+}
+
+zero_status_t plan_scalars_get(zero_plan_t plan, PlanScalars* out)
+{
+    const zero_status_t s = fetch_mirror(plan);
+    if (s != ZERO_OK) return s;
+    const DevScalars* sc = plan->h_mirror;
+    out->loss_scale = sc->loss_scale;
+    out->good_steps = sc->good_steps;
+    out->t = sc->t;
+    out->beta1_pow = sc->beta1_pow;
+    out->beta2_pow = sc->beta2_pow;
+    return ZERO_OK;
+}
+
+zero_status_t plan_scalars_set(zero_plan_t plan, const PlanScalars& in)
+{
+    if (plan->stepped && cudaEventSynchronize(plan->ev_done) != cudaSuccess) return ZERO_ECUDA;
+    DevScalars sc{};
+    sc.loss_scale = in.loss_scale;
+    sc.good_steps = in.good_steps;
+    sc.t = in.t;
+    sc.beta1_pow = in.beta1_pow;
+    sc.beta2_pow = in.beta2_pow;
+    DevStatus st{};
+    st.clip_coef = 1.0f;
+    st.used_scale = in.loss_scale;
+    std::memcpy(plan->h_mirror, &sc, sizeof(DevScalars));
+    std::memcpy(reinterpret_cast<char*>(plan->h_mirror) + sizeof(DevScalars), &st,
+                sizeof(DevStatus));
+    // DevState starts with the scalars and the status, in this order
+    cudaError_t e = cudaMemcpyAsync(plan->d_state, plan->h_mirror,
+                                    sizeof(DevScalars) + sizeof(DevStatus),
+                                    cudaMemcpyHostToDevice, plan->copy_stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(plan->copy_stream);
+    if (e != cudaSuccess) return ZERO_ECUDA;
+    plan->stepped = false;
+    std::fill(plan->bucket_seen.begin(), plan->bucket_seen.end(), 0);
+    return ZERO_OK;
+}
+
+void plan_set_poisoned(zero_plan_t plan, bool poisoned) { plan->poisoned = poisoned; }
+bool plan_poisoned(zero_plan_t plan) { return plan->poisoned; }
+
+void* const* plan_staging(zero_plan_t plan, int count, uint64_t bytes)
+{
+    if ((int)plan->staging.size() >= count && plan->staging_bytes >= bytes)
+        return plan->staging.data();
+    for (void* b : plan->staging) cudaFreeHost(b);
+    plan->staging.clear();
+    plan->staging_bytes = 0;
+    for (int i = 0; i < count; i++) {
+        void* b = nullptr;
+        if (cudaHostAlloc(&b, bytes, cudaHostAllocDefault) != cudaSuccess) {
+            for (void* q : plan->staging) cudaFreeHost(q);
+            plan->staging.clear();
+            return nullptr;
+        }
+        plan->staging.push_back(b);
+    }
+    plan->staging_bytes = bytes;
+    return plan->staging.data();
+}
+
 const void* step_kernel(int dtype, int kind, int nd)
 {
     return dtype == 0 ? step_kernel_fp16(kind, nd) : step_kernel_bf16(kind, nd);
@@ -449,6 +554,7 @@ zero_status_t zero_step_bucket(zero_plan_t plan, uint64_t bucket, const void* bu
                                void* workspace, void* stream)
 {
     if (!plan || plan->bucket_elems == 0 || bucket >= plan->nbuckets) return ZERO_EINVAL;
+    if (plan->poisoned) return ZERO_ESTATE;
     if (!bucket_grads || !aligned16(bucket_grads) || !workspace || !aligned16(workspace))
         return ZERO_EINVAL;
     if (plan->bucket_seen[(size_t)bucket]) return ZERO_EINVAL;        // once per step
@@ -481,6 +587,7 @@ zero_status_t zero_step_apply(zero_plan_t plan, float* master, float* m, float* 
                               void* workspace, void* stream)
 {
     if (!plan || plan->bucket_elems == 0) return ZERO_EINVAL;
+    if (plan->poisoned) return ZERO_ESTATE;
     for (uint8_t seen : plan->bucket_seen)
         if (!seen) return ZERO_EINVAL;                                 // a bucket is missing
     if (plan->n > 0) {
@@ -554,6 +661,7 @@ zero_status_t zero_step(zero_plan_t plan, const void* grads, float* master, floa
                         void* params, void* workspace, void* stream)
 {
     if (!plan) return ZERO_EINVAL;
+    if (plan->poisoned) return ZERO_ESTATE;
     if (plan->n > 0) {
         const void* ptrs[] = {grads, master, m, v, params};
         for (const void* q : ptrs)
@@ -629,6 +737,7 @@ zero_status_t zero_gather_layer(zero_plan_t plan, int unit, const void* const* s
 {
     if (!plan || plan->stage != 3 || unit < 0 || unit >= (int)plan->unit_len.size())
         return ZERO_EINVAL;
+    if (plan->poisoned) return ZERO_ESTATE;
     if (!shard_ptrs || !out || !aligned16(out)) return ZERO_EINVAL;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return ZERO_ECUDA;
@@ -706,6 +815,10 @@ const char* zero_status_string(zero_status_t status)
     case ZERO_ENOMEM: return "ZERO_ENOMEM: allocation failed";
     case ZERO_ECUDA: return "ZERO_ECUDA: CUDA call failed";
     case ZERO_ETIMEOUT: return "ZERO_ETIMEOUT: bounded device wait gave up";
+    case ZERO_ENOENT: return "ZERO_ENOENT: a checkpoint file is missing";
+    case ZERO_ECORRUPT: return "ZERO_ECORRUPT: a checkpoint file is damaged or does not belong";
+    case ZERO_EIO: return "ZERO_EIO: reading or writing a file failed";
+    case ZERO_ESTATE: return "ZERO_ESTATE: a failed checkpoint load left the state incomplete";
     default: return "unknown zero_status_t";
     }
 }

@@ -12,6 +12,7 @@
 
 #include "zero_b200.h"
 #include "zero_launch.h"
+#include "zero_plan_access.h"
 
 namespace zero {
 
@@ -197,19 +198,13 @@ extern "C" zero_status_t zero_quantize_shard(zero_dtype_t dtype, const void* sha
     return ZERO_OK;
 }
 
-// Plan fields this file needs (the plan is defined in zero_abi.cu).
-namespace zero {
-int plan_nd(zero_plan_t plan);
-int plan_stage(zero_plan_t plan);
-int plan_dtype(zero_plan_t plan);
-}  // namespace zero
-
 extern "C" zero_status_t zero_gather_layer_q(zero_plan_t plan, int unit, int bits,
                                              const void* const* code_ptrs,
                                              const float* const* scale_ptrs, void* out,
                                              void* stream)
 {
     if (!plan || plan_stage(plan) != 3 || (bits != 8 && bits != 4)) return ZERO_EINVAL;
+    if (plan_poisoned(plan)) return ZERO_ESTATE;
     uint64_t len = 0, slice = 0, off = 0;
     if (zero_plan_unit(plan, unit, &len, &slice, &off) != ZERO_OK) return ZERO_EINVAL;
     if (!code_ptrs || !scale_ptrs || !out || !aligned_to(out, 16)) return ZERO_EINVAL;
