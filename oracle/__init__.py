@@ -133,6 +133,10 @@ def lib():
                 "zo_layout_shard_len": (_I64, [_P]),
                 "zo_layout_global": (_I64, [_P, ctypes.c_int, _I64]),
                 "zo_reshard": (None, [_P, _P, _P, _P, ctypes.c_int]),
+                "zo_reduce16": (ctypes.c_int, [ctypes.c_int, _I64, ctypes.c_int, _P, _I64,
+                                               ctypes.c_float, _P, _P]),
+                "zo_step_offload": (ctypes.c_int, [ctypes.c_int, _I64, ctypes.c_int, _P, _P, _P,
+                                                   _P, _P, _P, _P, _P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -221,6 +225,32 @@ def step(nd, dtype, grads, master, m, v, params, opt: Opt, st: Scalars) -> dict:
                        ctypes.addressof(hp), ctypes.addressof(st), ctypes.addressof(res))
     if rc != 0:
         raise MemoryError("oracle step: allocation failed")
+    return res.as_dict()
+
+
+def reduce16(nd, dtype, grads, loss_scale=1.0, n=None, rank_stride=None):
+    """The offloaded reduce: returns (g16 uint16[n] as copied to the host,
+    g float32[n] unscaled on the host, overflow)."""
+    grads = np.ascontiguousarray(grads, dtype=np.uint16)
+    rs = grads.shape[-1] if rank_stride is None else rank_stride
+    n = rs if n is None else n
+    g16 = np.empty(n, np.uint16)
+    g = np.empty(n, np.float32)
+    ovf = lib().zo_reduce16(nd, n, dtype, _ptr(grads), rs, loss_scale, _ptr(g16), _ptr(g))
+    return g16, g, bool(ovf)
+
+
+def step_offload(nd, dtype, grads, master, m, v, params, opt: Opt, st: Scalars) -> dict:
+    """One ZeRO-Offload step; updates master/m/v/params/st in place."""
+    grads = np.ascontiguousarray(grads, dtype=np.uint16)
+    n = master.size
+    assert grads.shape == (nd, n) and m.size == n and v.size == n and params.size == n
+    hp, res = opt.c(), Result()
+    rc = lib().zo_step_offload(nd, n, dtype, _ptr(grads), _ptr(master), _ptr(m), _ptr(v),
+                               _ptr(params), ctypes.addressof(hp), ctypes.addressof(st),
+                               ctypes.addressof(res))
+    if rc != 0:
+        raise MemoryError("oracle offload step: allocation failed")
     return res.as_dict()
 
 

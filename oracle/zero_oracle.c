@@ -556,3 +556,48 @@ void zo_reshard(const zo_layout* A, const void* const* old_shards, const zo_layo
         }
     free(flat);
 }
+
+/* ======================================================================
+ * ZeRO-Offload: the reduced gradient is copied to the host in the 16-bit
+ * type and the host runs the update ([L18] sec. 4.4; [ZL8] sec. 6.2, 7).
+ * ====================================================================== */
+int zo_reduce16(int nd, int64_t n, int dtype, const uint16_t* grads, int64_t rank_stride,
+                float loss_scale, uint16_t* g16, float* g)
+{
+    int bad = 0;
+    for (int64_t i = 0; i < n; i++) {
+        float sum = 0.0f;
+        for (int k = 0; k < nd; k++)
+            sum = sum + to_float(dtype, grads[(int64_t)k * rank_stride + i]);
+        float mean = sum / (float)nd;
+        uint16_t q = from_float(dtype, mean);            /* what crosses the link */
+        float gi = to_float(dtype, q) / loss_scale;      /* unscaled on the host  */
+        if (!isfinite(gi)) bad = 1;
+        g16[i] = q;
+        g[i] = gi;
+    }
+    return bad;
+}
+
+int zo_step_offload(int nd, int64_t n, int dtype, const uint16_t* grads,
+                    float* master, float* m, float* v, uint16_t* params,
+                    const zo_hparams* hp, zo_scalars* st, zo_result* res)
+{
+    size_t cnt = (size_t)(n > 0 ? n : 1);
+    float* g = (float*)malloc(cnt * sizeof(float));
+    uint16_t* q = (uint16_t*)malloc(cnt * sizeof(uint16_t));
+    if (!g || !q) {
+        free(g);
+        free(q);
+        return -1;
+    }
+    int bad = zo_reduce16(nd, n, dtype, grads, n, st->loss_scale, q, g);
+    res->grad_norm = sqrt(zo_sumsq(n, g));
+    res->clip_coef = zo_clip_coef(res->grad_norm, hp->clip_norm);
+    zo_advance(hp, st, bad, res);
+    if (!res->skipped)
+        zo_adam(n, g, res->clip_coef, master, m, v, params, dtype, hp, res->bc1, res->bc2);
+    free(g);
+    free(q);
+    return 0;
+}

@@ -159,6 +159,24 @@ void zo_gather_unit_q(int dtype, int nd, int64_t len, int64_t slice, int64_t off
                       int64_t block, const uint8_t* const* q, const float* const* scales,
                       uint16_t* out);
 
+/* ---- ZeRO-Offload ([L18] sec. 4.4: the fp32 master, m and v and the Adam
+ *      update live on the host; each step moves the 16-bit gradients to the
+ *      host, 2 Psi, and the 16-bit parameters back, 2 Psi; [ZL8] sec. 6.2, 7:
+ *      the device runs forward and backward, the host the parameter update) --
+ * The reduced gradient crosses the link in the 16-bit type: the rank-order
+ * fp32 fold divided by nd is rounded to the 16-bit type (that is what is
+ * copied), and the host unscales the copied value:
+ *   g16[i] = to16(fold_i / nd);   g[i] = (float)g16[i] / loss_scale.
+ * Returns 1 if any g[i] is inf or NaN.  grads: [nd][rank_stride]. */
+int zo_reduce16(int nd, int64_t n, int dtype, const uint16_t* grads, int64_t rank_stride,
+                float loss_scale, uint16_t* g16, float* g);
+/* One offloaded step: zo_reduce16, then the norm, clip, skip decision and
+ * Adam exactly as zo_step, on the host's master, m, v; params receives the
+ * 16-bit parameters copied back to the device. */
+int zo_step_offload(int nd, int64_t n, int dtype, const uint16_t* grads,
+                    float* master, float* m, float* v, uint16_t* params,
+                    const zo_hparams* hp, zo_scalars* st, zo_result* res);
+
 /* ---- sharded checkpoint: ownership regrouped for another rank count
  *      ([Z026] sec. 5: restoring at a different degree of parallelism must
  *      reorganise which rank owns what while keeping the parameter order and

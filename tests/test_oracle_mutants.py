@@ -13,7 +13,8 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "zero_oracle.c")
 PIN_TESTS = ["tests/test_oracle_step.py", "tests/test_oracle_formats.py",
-             "tests/test_oracle_quant.py", "tests/test_oracle_ckpt.py"]
+             "tests/test_oracle_quant.py", "tests/test_oracle_ckpt.py",
+             "tests/test_oracle_offload.py"]
 
 MUTANTS = {
     "reduce-reverse-rank-order": ("for (int r = 0; r < nd; r++)\n            s = s +",
@@ -57,6 +58,14 @@ MUTANTS = {
     "layout-boundary-off-by-one": ("if (j < slice_start + s) {", "if (j <= slice_start + s) {"),
     "reshard-ranks-reversed": ("int64_t g = zo_layout_global(A, r, j);",
                                "int64_t g = zo_layout_global(A, A->nd - 1 - r, j);"),
+    "offload-no-rounding": ("float gi = to_float(dtype, q) / loss_scale;",
+                            "float gi = mean / loss_scale;"),
+    "offload-unscale-before-round": ("uint16_t q = from_float(dtype, mean);",
+                                     "uint16_t q = from_float(dtype, mean / loss_scale);"),
+    "offload-no-average": ("float mean = sum / (float)nd;", "float mean = sum;"),
+    "offload-clip-dropped": ("res->clip_coef = zo_clip_coef(res->grad_norm, hp->clip_norm);\n"
+                             "    zo_advance(hp, st, bad, res);",
+                             "res->clip_coef = 1.0f;\n    zo_advance(hp, st, bad, res);"),
 }
 
 
