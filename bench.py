@@ -839,6 +839,100 @@ def run_checkpoint(args):
         shutil.rmtree(d, ignore_errors=True)
 
 
+def host_copy_gbs(threads, nbytes=4 << 30):
+    """Host memory bandwidth for scale: `threads` threads each copying their slice
+    of an nbytes array (numpy copies release the GIL); read + write bytes / s."""
+    import numpy as np
+    from concurrent.futures import ThreadPoolExecutor
+    src = np.ones(nbytes // 4, np.float32)
+    dst = np.empty_like(src)
+    parts = np.array_split(np.arange(src.size), threads)
+    bounds = [(int(p[0]), int(p[-1]) + 1) for p in parts if p.size]
+
+    def one(b):
+        np.copyto(dst[b[0]:b[1]], src[b[0]:b[1]])
+
+    with ThreadPoolExecutor(threads) as ex:
+        list(ex.map(one, bounds))                   # first touch
+        best = 0.0
+        for _ in range(3):
+            t0 = time.perf_counter()
+            list(ex.map(one, bounds))
+            best = max(best, 2 * nbytes / (time.perf_counter() - t0) / 1e9)
+    return best
+
+
+def run_offload(args):
+    """ZeRO-Offload on the workload: the device reduce (16-bit averaged gradient),
+    the copy to the host, the host Adam on host-resident master, m, v and the
+    16-bit parameters back, through zero_offload_step; and the host Adam alone
+    (zero_cpu_adam).  Wall clock around the synchronous calls."""
+    import numpy as np
+    import torch
+    import gen
+    import zero_sharded_mixed_02_gb300 as z
+    from zero_sharded_mixed_02_gb300 import build as zbuild
+    zbuild.build()
+    w = workload(args.psi, args.workload)
+    if w.stage == 3:
+        print(json.dumps({"mode": "offload", "workload": w.name,
+                          "unavailable": "offload runs on stages 0-2 plans"}), flush=True)
+        return
+    dev = torch.device("cuda", 0)
+    plan = _plan_for(z, w)
+    threads = args.host_threads or os.cpu_count()
+    try:
+        _, padded, _, _ = z.zero_plan_layout(plan)
+        n = w.psi
+        d = torch.zeros(padded, dtype=torch.float32, device=dev)
+        gen.cuda_f32(d.data_ptr(), 0, gen.STREAM_MASTER, 0, 0, n, 0.02)
+        master = d.cpu().numpy()
+        del d
+        m = np.zeros(padded, np.float32)
+        v = np.zeros(padded, np.float32)
+        params = torch.zeros(padded, dtype=torch.int16, device=dev)
+        work = torch.empty(padded, dtype=torch.int16, device=dev)
+        grads = torch.empty((w.nd, padded), dtype=torch.int16, device=dev)
+        gen.cuda_ranks_16(grads.data_ptr(), 0, gen.STREAM_GRAD, 1, w.nd, n, w.grad_sigma,
+                          w.loss_scale, w.dtype, rank_stride=padded)
+        torch.cuda.synchronize()
+        stream = torch.cuda.current_stream().cuda_stream
+        for _ in range(max(1, args.warmup)):
+            z.zero_offload_step(plan, grads, master, m, v, params, work, threads, stream)
+        K = max(2, min(args.steps, 5))
+        t0 = time.perf_counter()
+        for _ in range(K):
+            z.zero_offload_step(plan, grads, master, m, v, params, work, threads, stream)
+        t_step = (time.perf_counter() - t0) / K
+        r = z.zero_step_result(plan)
+        # the host Adam alone, on the last copied gradient
+        g16 = work[:n].cpu().numpy()
+        p16 = np.empty(n, np.uint16)
+        hp = z.hparams(**w.hparams())
+        z.zero_cpu_adam(g16, w.dtype, n, r["loss_scale"], 1.0, 0.5, 0.5, hp, master, m, v,
+                        p16, threads)
+        t0 = time.perf_counter()
+        for _ in range(K):
+            z.zero_cpu_adam(g16, w.dtype, n, r["loss_scale"], 1.0, 0.5, 0.5, hp, master, m, v,
+                            p16, threads)
+        t_adam = (time.perf_counter() - t0) / K
+        bw = host_copy_gbs(threads)
+        host_bytes = 28 * n          # g16 2 + master/m/v 12 read, 12 written, params 2 written
+        print(json.dumps({
+            "mode": "offload", "workload": f"{w.name}: {DESCRIPTIONS.get(w.name, w.name)}",
+            "psi": n, "nd": w.nd, "host_threads": threads,
+            "offload_step_ms": t_step * 1e3, "offload_step_params_per_s": n / t_step,
+            "host_adam_ms": t_adam * 1e3, "host_adam_params_per_s": n / t_adam,
+            "pages_cpu_adam_params_per_s": 1.5e9,
+            "host_adam_vs_pages": n / t_adam / 1.5e9,
+            "host_adam_gbs": host_bytes / t_adam / 1e9, "host_copy_gbs_measured": bw,
+            "host_adam_frac_of_copy": host_bytes / t_adam / 1e9 / bw,
+            "link_bytes_per_step": 4 * n, "step_result": r,
+            "timing": "host wall clock around the synchronous calls"}), flush=True)
+    finally:
+        z.zero_plan_destroy(plan)
+
+
 # ------------------------------------------------------------ reference arm
 def run_reference(args):
     """The CPU oracle, as it stands, on the host cores: each step is one oracle
@@ -885,6 +979,9 @@ def main(argv=None):
     ap.add_argument("--workload", choices=WORKLOADS, default="gpt2-1.5b")
     ap.add_argument("--sweep", action="store_true",
                     help="bandwidth sweep: one JSON line per (psi, nd) point")
+    ap.add_argument("--offload", action="store_true",
+                    help="time ZeRO-Offload steps (device reduce, host Adam) on the workload")
+    ap.add_argument("--host-threads", type=int, default=0, help="host threads for --offload")
     ap.add_argument("--checkpoint", action="store_true",
                     help="time a sharded checkpoint save and a resharding load of the workload")
     ap.add_argument("--ckpt-dir", default=None, help="where --checkpoint writes (default: tmp)")
@@ -904,6 +1001,8 @@ def main(argv=None):
         run_buckets(args)
     elif args.checkpoint:
         run_checkpoint(args)
+    elif args.offload:
+        run_offload(args)
     elif args.workload == "llama3-8b":
         run_stage3(args)
     else:

@@ -361,6 +361,48 @@ zero_status_t zero_checkpoint_save(zero_plan_t plan, const char* dir, int rank,
 zero_status_t zero_checkpoint_load(zero_plan_t plan, const char* dir, int rank, float* master,
                                    float* m, float* v, void* params, void* stream);
 
+/* ---- ZeRO-Offload: the Adam update on the host ------------------------------- */
+/* [L18] sec. 4.4: the device keeps the 16-bit parameters and gradients; the
+ * host keeps the fp32 master, m and v and runs Adam, multithreaded and
+ * vectorised; each step copies the 16-bit gradients to the host (2 psi bytes)
+ * and the updated 16-bit parameters back (2 psi).  [ZL8] sec. 6.2, 7: the
+ * device runs forward and backward, the host the parameter update. */
+
+/* One offloaded step of a stages 0-2 plan.  On the device: the rank-order fp32
+ * fold of the nd contributions divided by nd, rounded to the plan's 16-bit
+ * type (the copied value; written to `workspace`), the overflow flag and the
+ * global norm of that value divided by the loss scale, and the step's
+ * scalars (skip, clip coefficient, loss-scale update, t, bias corrections), as
+ * zero_step.  On the host, unless the step is skipped: g = copied value / S,
+ * times the clip coefficient, then Adam/AdamW on master, m, v exactly as
+ * zero_step's update, and the 16-bit parameters copied to `params`.
+ *   grads      device [nd][nd*S] 16-bit, as zero_step.
+ *   master,m,v HOST fp32 arrays of at least psi elements (elements >= psi
+ *              untouched); pageable or pinned.
+ *   params     device [nd*S] 16-bit flat parameters (elements >= psi untouched).
+ *   workspace  device scratch of at least 2*psi bytes, 16-byte aligned.
+ *   nthreads   host threads (<= 0: one per hardware thread).
+ * The copies stream through the plan's pinned staging in 2^24-element chunks
+ * overlapped with the host arithmetic.  Synchronous: returns when the
+ * parameters are on the device.  zero_step_result reports the step.
+ * Errors: ZERO_EINVAL (stage 3, null or misaligned pointer), ZERO_ESTATE,
+ * ZERO_ENOMEM, ZERO_ECUDA. */
+zero_status_t zero_offload_step(zero_plan_t plan, const void* grads, float* master, float* m,
+                                float* v, void* params, void* workspace, int nthreads,
+                                void* stream);
+
+/* The host Adam alone, on host memory: for i < n, g = grads16[i] (the 16-bit
+ * type `dtype`) / loss_scale * clip_coef, then Adam/AdamW with the bias
+ * corrections bc1 = 1 - beta1^t and bc2 = 1 - beta2^t of this step, each
+ * operation one binary32 rounding in the order of zero_step's update; master,
+ * m, v updated in place, params16[i] = master[i] rounded to the 16-bit type.
+ * nthreads <= 0: one thread per hardware thread.  Needs no GPU.
+ * Errors: ZERO_EINVAL (null pointer, dtype, loss_scale/bc1/bc2 not > 0),
+ * ZERO_ENOMEM. */
+zero_status_t zero_cpu_adam(const void* grads16, zero_dtype_t dtype, uint64_t n, float loss_scale,
+                            float clip_coef, float bc1, float bc2, const zero_hparams_t* hp,
+                            float* master, float* m, float* v, void* params16, int nthreads);
+
 /* ---- memory ledger and communication volume ------------------------------- */
 
 /* Bytes of model state one rank holds ([L18] 1.2, 2.1; [Z026] 2; [L32] 2.1,

@@ -36,7 +36,7 @@ ENTRY_POINTS = (
     "zero_status_string", "zero_plan_profile", "zero_plan_kernel_times", "zero_plan_path",
     "zero_grad_norm_noalloc", "zero_plan_set_reduce_kernel", "zero_quantize_shard",
     "zero_gather_layer_q", "zero_plan_set_bucket", "zero_step_bucket", "zero_step_apply",
-    "zero_checkpoint_save", "zero_checkpoint_load",
+    "zero_checkpoint_save", "zero_checkpoint_load", "zero_offload_step", "zero_cpu_adam",
 )
 
 
@@ -112,6 +112,10 @@ def lib():
                                               ctypes.c_int, _P]),
                 "zero_checkpoint_load": (st, [_P, ctypes.c_char_p, ctypes.c_int, _P, _P, _P, _P,
                                               _P]),
+                "zero_offload_step": (st, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_int, _P]),
+                "zero_cpu_adam": (st, [_P, ctypes.c_int, _U64, ctypes.c_float, ctypes.c_float,
+                                       ctypes.c_float, ctypes.c_float, _P, _P, _P, _P, _P,
+                                       ctypes.c_int]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -126,6 +130,15 @@ def _ptr(x) -> Optional[int]:
     if hasattr(x, "data_ptr"):
         return x.data_ptr()
     return int(x)
+
+
+def _hptr(x) -> Optional[int]:
+    """Address of a host array: a numpy array or a CPU tensor."""
+    if x is None:
+        return None
+    if hasattr(x, "__array_interface__"):
+        return x.__array_interface__["data"][0]
+    return _ptr(x)
 
 
 def _check(code: int, where: str):
@@ -257,6 +270,22 @@ def zero_checkpoint_load(plan: int, directory: str, rank: int, master, m, v, par
     _check(lib().zero_checkpoint_load(plan, os.fsencode(directory), rank, _ptr(master), _ptr(m),
                                       _ptr(v), _ptr(params), _ptr(stream)),
            "zero_checkpoint_load")
+
+
+def zero_offload_step(plan: int, grads, master, m, v, params, workspace, nthreads: int = 0,
+                      stream=0) -> None:
+    """master, m, v: host arrays (numpy float32 or CPU tensors); the rest device."""
+    _check(lib().zero_offload_step(plan, _ptr(grads), _hptr(master), _hptr(m), _hptr(v),
+                                   _ptr(params), _ptr(workspace), nthreads, _ptr(stream)),
+           "zero_offload_step")
+
+
+def zero_cpu_adam(grads16, dtype: int, n: int, loss_scale: float, clip_coef: float, bc1: float,
+                  bc2: float, hp, master, m, v, params16, nthreads: int = 0) -> None:
+    """Host arrays throughout (numpy or CPU tensors)."""
+    _check(lib().zero_cpu_adam(_hptr(grads16), dtype, n, loss_scale, clip_coef, bc1, bc2,
+                               ctypes.byref(hp), _hptr(master), _hptr(m), _hptr(v),
+                               _hptr(params16), nthreads), "zero_cpu_adam")
 
 
 def zero_quantize_shard(dtype: int, shard, n: int, bits: int, codes, scales, stream=0) -> None:

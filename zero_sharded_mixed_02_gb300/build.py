@@ -18,10 +18,18 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libzero_b200.so")
 
 SOURCES = ["zero_abi.cu", "zero_step_fp16.cu", "zero_step_bf16.cu", "zero_gather.cu",
-           "zero_noalloc.cu", "zero_qwz.cu", "zero_ckpt.cu"]
+           "zero_noalloc.cu", "zero_qwz.cu", "zero_ckpt.cu", "zero_offload.cu",
+           "zero_cpu_adam.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                      "-I", INCLUDE, "-I", CSRC]
+# Host-only sources (the ZeRO-Offload host Adam): every floating-point operation
+# rounded on its own (no fused multiply-add), which the element loop needs to
+# match the device update bit for bit; errno and trap assumptions relaxed so the
+# loop vectorises (neither changes a value).  No -march: the same flags build
+# on x86-64 and AArch64.
+HOST_FLAGS = ["-std=c++17", "-O3", "-ffp-contract=off", "-fno-math-errno", "-fno-trapping-math",
+              "-fPIC", "-pthread", "-Wall", "-I", INCLUDE, "-I", CSRC]
 
 
 def _inputs():
@@ -47,9 +55,12 @@ def build(force: bool = False, verbose: bool = False) -> str:
     procs = []
     objs = []
     for src in SOURCES:
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
         objs.append(obj)
-        cmd = ["nvcc", *NVCC_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        if src.endswith(".cpp"):
+            cmd = ["g++", *HOST_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        else:
+            cmd = ["nvcc", *NVCC_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd), file=sys.stderr)
         procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT,

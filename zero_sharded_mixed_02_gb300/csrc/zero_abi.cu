@@ -428,6 +428,40 @@ zero_status_t plan_scalars_set(zero_plan_t plan, const PlanScalars& in)
     return ZERO_OK;
 }
 
+zero_status_t plan_step_status(zero_plan_t plan, PlanStepStatus* out)
+{
+    const zero_status_t s = fetch_mirror(plan);
+    if (s != ZERO_OK) return s;
+    const DevStatus* st = reinterpret_cast<const DevStatus*>(
+        reinterpret_cast<const char*>(plan->h_mirror) + sizeof(DevScalars));
+    out->skipped = st->skipped;
+    out->overflow = st->overflow;
+    out->grad_norm = st->grad_norm;
+    out->clip_coef = st->clip_coef;
+    out->bc1 = st->bc1;
+    out->bc2 = st->bc2;
+    out->used_scale = st->used_scale;
+    return st->err ? ZERO_ETIMEOUT : ZERO_OK;
+}
+
+void plan_hparams(zero_plan_t plan, zero_hparams_t* out) { *out = plan->hp; }
+
+zero_status_t plan_launch_reduce16(zero_plan_t plan, const void* fn, const void* grads, void* g16,
+                                   void* stream)
+{
+    if (!fn) return ZERO_EINVAL;
+    StepArgs a = step_args(plan, grads, nullptr, nullptr, nullptr, nullptr, nullptr);
+    const int grid = grid_reduce(fn, plan->sms, plan->n, REDUCE_WAVES);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void* args[] = {&a, &g16};
+    if (cudaLaunchKernel(fn, dim3(grid), dim3(ZERO_THREADS), args, 0, s) != cudaSuccess)
+        return ZERO_ECUDA;
+    plan->launches++;
+    if (cudaEventRecord(plan->ev_done, s) != cudaSuccess) return ZERO_ECUDA;
+    plan->stepped = true;
+    return ZERO_OK;
+}
+
 void plan_set_poisoned(zero_plan_t plan, bool poisoned) { plan->poisoned = poisoned; }
 bool plan_poisoned(zero_plan_t plan) { return plan->poisoned; }
 

@@ -38,6 +38,21 @@ zero_status_t plan_scalars_get(zero_plan_t plan, PlanScalars* out);
 // Replaces them (and resets the last-step report to its before-any-step state).
 zero_status_t plan_scalars_set(zero_plan_t plan, const PlanScalars& sc);
 
+// What the last step's reduce pass settled (waits for it).
+struct PlanStepStatus {
+    int skipped = 0, overflow = 0;
+    double grad_norm = 0.0;
+    float clip_coef = 1.0f, bc1 = 0.0f, bc2 = 0.0f, used_scale = 1.0f;
+};
+zero_status_t plan_step_status(zero_plan_t plan, PlanStepStatus* out);
+void plan_hparams(zero_plan_t plan, zero_hparams_t* out);
+
+// Launch `fn`, a reduce-pass kernel taking (StepArgs, uint16_t* g16), over the
+// plan's gradients as the step's reduce pass (the grid of the plain reduce
+// pass; the plan's step event recorded after it).
+zero_status_t plan_launch_reduce16(zero_plan_t plan, const void* fn, const void* grads, void* g16,
+                                   void* stream);
+
 // A plan whose state a failed load left half-written refuses steps and gathers.
 void plan_set_poisoned(zero_plan_t plan, bool poisoned);
 bool plan_poisoned(zero_plan_t plan);
