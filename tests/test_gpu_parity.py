@@ -184,6 +184,20 @@ def test_deterministic_rerun(z):
     assert [r["grad_norm"] for r in a.results] == [r["grad_norm"] for r in b.results]
 
 
+@pytest.mark.parametrize("nd", [3, 8])
+def test_stages_0_1_2_are_bitwise_identical(z, nd):
+    """Plain DP, ZeRO-1 and ZeRO-2 differ only in what each rank keeps in memory
+    ([L18] 2.1-2.3): the step's results are the same bits."""
+    c = H.Case(shapes=[(300_001,), (77,)], nd=nd, dtype=gen.FP16, grad_sigma=1e-3,
+               loss_scale=4096.0, dynamic_scale=1, clip=0.5, steps=3, inf_steps=(2,))
+    runs = [H.run_gpu(z, dataclasses.replace(c, stage=s)) for s in (0, 1, 2)]
+    for r in runs[1:]:
+        for x, y in zip((runs[0].master, runs[0].m, runs[0].v, runs[0].params),
+                        (r.master, r.m, r.v, r.params)):
+            assert x.tobytes() == y.tobytes()
+        assert r.results == runs[0].results
+
+
 def test_misaligned_and_missing_pointers_rejected(z):
     import torch
     c = H.Case(shapes=[(4096,)], nd=4, clip=1.0)

@@ -351,3 +351,70 @@ def test_gather_inverts_shard(oracle, nd, length):
     flat = np.concatenate(slices)
     assert np.array_equal(flat[:length], unit) and not flat[length:].any()
     assert np.array_equal(oracle.gather_unit(nd, length, slice_elems, slices), unit)
+
+
+# ------------------------------------------- brute force against the textbook
+def textbook_steps(nd, dtype, grads_per_step, master, S, clip, lr, wd, b1f, b2f, eps):
+    """Mixed-precision Adam/AdamW steps of the pages' method written out in
+    float64 (16-bit inputs exact in float64; every operation ~1e-16 relative),
+    with the fp16 dynamic loss scale (skip and halve on overflow)."""
+    p = master.astype(np.float64)
+    m = np.zeros_like(p)
+    v = np.zeros_like(p)
+    t, out = 0, []
+    b1, b2 = float(b1f), float(b2f)
+    for g16 in grads_per_step:
+        x = np.stack([val16(dtype, g16[r]) for r in range(nd)])
+        g = x.sum(axis=0) / nd / S
+        if not np.all(np.isfinite(g)):
+            S = S / 2
+            out.append(("skip", S))
+            continue
+        norm = math.sqrt(float(np.sum(g * g)))
+        c = clip / norm if clip > 0 and norm > clip else 1.0
+        t += 1
+        bc1, bc2 = 1.0 - b1 ** t, 1.0 - b2 ** t
+        p = p * (1.0 - lr * wd)
+        m = b1 * m + (1.0 - b1) * (g * c)
+        v = b2 * v + (1.0 - b2) * (g * c) ** 2
+        p = p - lr * (m / bc1) / (np.sqrt(v / bc2) + eps)
+        out.append(("step", norm))
+    return p, m, v, S, out
+
+
+@pytest.mark.parametrize("n", [5, 13, 16])
+@pytest.mark.parametrize("nd", [1, 2, 3, 4, 8, 16])
+def test_brute_force_against_the_textbook(oracle, n, nd):
+    """Tiny models, every rank count of the configurations: three steps (the
+    second with an injected inf) of the oracle against the float64 textbook.
+    The oracle rounds each binary32 operation, so the two agree to a few
+    binary32 ulps on master, m, v and to 1 ulp on the 16-bit params."""
+    rng = np.random.default_rng(100 * n + nd)
+    S, clip, lr, wd = 1024.0, 0.05, 1e-3, 0.01
+    steps = []
+    for k in range(3):
+        g = f16(rng.standard_normal((nd, n)) * 1e-2 * S)
+        if k == 1:
+            g[nd - 1, n // 2] = 0x7C00
+        steps.append(g)
+    master0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    opt = oracle.Opt(lr=lr, weight_decay=wd, decoupled_wd=1, clip_norm=clip, dynamic_scale=1)
+    st = oracle.new_scalars(S)
+    master, m, v, params = master0.copy(), *state(n)[1:]
+    res = [oracle.step(nd, FP16, g, master, m, v, params, opt, st) for g in steps]
+    tp, tm, tv, tS, tout = textbook_steps(nd, FP16, steps, master0, S, clip, lr, wd,
+                                          np.float32(0.9), np.float32(0.999), np.float32(1e-8))
+    assert [r["skipped"] for r in res] == [0, 1, 0] and [o[0] for o in tout] == ["step", "skip", "step"]
+    assert st.loss_scale == tS == S / 2 and st.t == 2
+    for r, o in zip(res, tout):
+        if o[0] == "step":
+            # each g is one binary32 rounding (or two: fold, divide) off the real value
+            assert abs(r["grad_norm"] - o[1]) <= 1e-6 * o[1]
+    # a few binary32 ulps: 1e-5 relative, plus 1e-6 of the array's largest value
+    # where the update nearly cancels the old value (a dropped term or a wrong
+    # sign is off by about lr = 1e-3 of the master's scale)
+    for got, want in ((master, tp), (m, tm), (v, tv)):
+        err = np.abs(got.astype(np.float64) - want)
+        assert np.all(err <= 1e-5 * np.abs(want) + 1e-6 * np.abs(want).max()), err.max()
+    keys = lambda b: np.where(b & 0x8000, -(b & 0x7FFF).astype(np.int32), (b & 0x7FFF).astype(np.int32))
+    assert np.max(np.abs(keys(params) - keys(f16(tp)))) <= 1
