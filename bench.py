@@ -21,6 +21,7 @@ exchange between GPUs here): weak scaling, barrier + max-over-ranks timing.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -209,16 +210,18 @@ def metric_of(w):
     return f"sharded Adam step params/s and HBM GB/s vs GB300 peak ({w.name}, Nd={w.nd})"
 
 
-def workload(psi=None, name="gpt2-1.5b"):
+def workload(psi=None, name="gpt2-1.5b", nd=None):
     """The GPT-2 1.5B workload (default) or another named one; with psi, a flat
     single-tensor model of psi parameters under the same settings (small cases
-    for profiling)."""
+    for profiling), with nd ranks when nd is given."""
     import dataclasses
     from gen import workloads
     w = {"gpt2-1.5b": workloads.gpt2_xl, "gpt2-small": workloads.gpt2_small,
          "tiny": workloads.tiny, "llama3-8b": workloads.llama3_8b}[name]()
     if psi:
         w = dataclasses.replace(w, name=f"flat-{psi}", shapes=[(psi,)])
+    if nd:
+        w = dataclasses.replace(w, nd=nd)
     return w
 
 
@@ -295,7 +298,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     zbuild.build()
-    w = workload(args.psi, args.workload)
+    w = workload(args.psi, args.workload, args.nd)
     hp = z.hparams(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
                    decoupled_wd=w.decoupled_wd, clip_norm=w.clip, loss_scale=w.loss_scale,
                    dynamic_scale=w.dynamic_scale, backoff=0.5, growth_interval=1000)
@@ -515,8 +518,8 @@ def run_sweep(args):
     sp = stream.cuda_stream
     peak, _ = measured_peaks()
     l2 = torch.empty(1 << 28, dtype=torch.uint8, device=dev)          # 256 MB > L2
-    for psi in W.SWEEP_PSI:
-        for nd in W.SWEEP_ND:
+    for psi in ([args.psi] if args.psi else W.SWEEP_PSI):
+        for nd in ([args.nd] if args.nd else W.SWEEP_ND):
             w = W.sweep(psi, nd)
             line = {"mode": "sweep", "metric": "sharded Adam step HBM GB/s, bandwidth sweep",
                     "psi": psi, "nd": nd, "zero_stage": 2, "dtype": "bf16 grads, f32 state"}
@@ -565,6 +568,11 @@ def run_stage3(args):
     from zero_sharded_mixed_02_gb300 import build as zbuild
     zbuild.build()
     w = workload(name="llama3-8b")
+    if args.layers or args.vocab:
+        from gen import workloads as W
+        w = W.scaled_llama(args.layers or 32, 4096, 14336, 32, 8, args.vocab or 128256, w.nd, w)
+    if args.nd:
+        w = dataclasses.replace(w, nd=args.nd)
     dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
@@ -628,9 +636,10 @@ def run_stage3(args):
                "gbs": q_bytes / (t_q / 1e3) / 1e9,
                "vs_unquantized_gather": t_gat / t_q,
                "frac_of_measured_hbm": q_bytes / (t_q / 1e3) / 1e9 / peak}
+    desc = DESCRIPTIONS.get(w.name, f"LLaMA-3-8B-shaped list scaled to {len(units) - 2} layers")
     print(json.dumps({
         "mode": "zero3", "metric": "ZeRO-3 step: resident-shard update and per-unit gathers",
-        "workload": f"{w.name}: {DESCRIPTIONS[w.name]}, {len(w.shapes)} tensors, {nunits} units",
+        "workload": f"{w.name}: {desc}, {len(w.shapes)} tensors, {nunits} units",
         "psi": w.psi, "nd": w.nd, "shard_elems": total, "steps": K,
         "update_ms": t_upd, "update_params_per_s": total / (t_upd / 1e3),
         "update_gbs": upd_bytes / (t_upd / 1e3) / 1e9, "update_bytes_per_elem": 2 * w.nd + 26,
@@ -639,7 +648,8 @@ def run_stage3(args):
         "frac_of_measured_hbm": {"update": upd_bytes / (t_upd / 1e3) / 1e9 / peak,
                                  "gather": gat_bytes / (t_gat / 1e3) / 1e9 / peak},
         "qwz": qwz or None,
-        "l2": "inputs larger than L2 (16 GB gradients, 16 GB shards)"}), flush=True)
+        "l2": (f"inputs larger than L2 ({2 * w.nd * total / 1e9:.1f} GB gradients, "
+               f"{2 * (w.nd - 1) * total / 1e9:.1f} GB shards)")}), flush=True)
     z.zero_plan_destroy(plan)
 
 
@@ -654,7 +664,7 @@ def run_buckets(args):
     import zero_sharded_mixed_02_gb300 as z
     from zero_sharded_mixed_02_gb300 import build as zbuild
     zbuild.build()
-    w = workload(args.psi, args.workload)
+    w = workload(args.psi, args.workload, args.nd)
     dev = torch.device("cuda", 0)
     peak, _ = measured_peaks()
     plan = _plan_for(z, w)
@@ -746,7 +756,7 @@ def run_checkpoint(args):
     import zero_sharded_mixed_02_gb300 as z
     from zero_sharded_mixed_02_gb300 import build as zbuild
     zbuild.build()
-    w = workload(args.psi, args.workload)
+    w = workload(args.psi, args.workload, args.nd)
     if w.stage == 3:
         print(json.dumps({"mode": "checkpoint", "workload": w.name,
                           "unavailable": "a ZeRO-3 plan holds one rank's shard; this mode "
@@ -873,7 +883,7 @@ def run_offload(args):
     import zero_sharded_mixed_02_gb300 as z
     from zero_sharded_mixed_02_gb300 import build as zbuild
     zbuild.build()
-    w = workload(args.psi, args.workload)
+    w = workload(args.psi, args.workload, args.nd)
     if w.stage == 3:
         print(json.dumps({"mode": "offload", "workload": w.name,
                           "unavailable": "offload runs on stages 0-2 plans"}), flush=True)
@@ -940,7 +950,7 @@ def run_reference(args):
     rank, _, ws = dist_env()
     if rank != 0:
         return
-    w = workload(args.psi, args.workload)
+    w = workload(args.psi, args.workload, args.nd)
     thr = oracle_threads(w.nd)
     n_s = args.ref_sample
     import oracle
@@ -990,7 +1000,15 @@ def main(argv=None):
     ap.add_argument("--qwz", type=int, choices=(0, 4, 8), default=0,
                     help="ZeRO-3 workload: also time the quantized (qwZ) gather at this width")
     ap.add_argument("--psi", type=int, default=0,
-                    help="flat model of this many parameters (profiling small cases)")
+                    help="flat model of this many parameters (profiling small cases); "
+                         "with --sweep, this one psi")
+    ap.add_argument("--nd", type=int, default=0,
+                    help="ranks of the --psi flat model or the llama3-8b workload; "
+                         "with --sweep, this one nd")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="llama3-8b workload: this many transformer layers (small cases)")
+    ap.add_argument("--vocab", type=int, default=0,
+                    help="llama3-8b workload: this vocabulary size (small cases)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)          # at least 3 untimed warm-up steps
     if args.impl == "reference":
