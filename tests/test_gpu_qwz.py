@@ -49,10 +49,107 @@ def test_quantize_shard_bitwise(env, n, bits, dtype):
     assert np.array_equal(codes.cpu().numpy()[:q.size], q)
 
 
+def _quantize_on_gpu(torch, z, dtype, x16, bits):
+    n = x16.size
+    d = torch.from_numpy(x16.view(np.int16)).cuda()
+    codes, scales = dev_codes(torch, n, bits)
+    z.zero_quantize_shard(dtype, d, n, bits, codes, scales,
+                          torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    return codes.cpu().numpy(), scales.cpu().numpy()
+
+
 @pytest.mark.parametrize("bits", [8, 4])
-def test_quantized_unit_gather_bitwise(env, bits):
+@pytest.mark.parametrize("dtype", [gen.FP16, gen.BF16])
+def test_quantize_exact_ties_round_to_even(env, bits, dtype):
+    """Blocks whose scale is a power of two and whose values are odd multiples of
+    half that scale: every quotient is an exact tie k + 1/2, which must go to the
+    even integer.  Values one 16-bit step either side of a tie are mixed in."""
     torch, z = env
-    w = W.scaled_llama(2, 256, 512, 8, 2, 1000, 16, W.llama3_8b())
+    qmax = 127 if bits == 8 else 7
+    rng = np.random.default_rng(100 + bits + dtype)
+    nblk = 48
+    x = np.empty(nblk * 256, np.float32)
+    for b in range(nblk):
+        scale = 2.0 ** (b % 20 - 10)
+        k = rng.integers(-qmax, qmax, 256)                    # k + 1/2 in [-qmax + 1/2, qmax - 1/2]
+        blk = (k + 0.5) * scale
+        blk[rng.integers(0, 256)] = qmax * scale * (1 if b % 2 else -1)   # sets max|x|
+        x[b * 256:(b + 1) * 256] = blk
+    x16 = oracle.from_float(dtype, x)
+    assert np.array_equal(oracle.to_float(dtype, x16), x)     # every value exact in 16 bits
+    step = np.where(rng.random(x16.size) < 0.1, rng.choice([-1, 1], x16.size), 0)
+    amax_pos = np.abs(x) == np.repeat(np.abs(x.reshape(nblk, 256)).max(1), 256)
+    x16 = np.where(amax_pos, x16, (x16.astype(np.int32) + step).astype(np.uint16))
+    q, s = oracle.quantize_16(dtype, x16, bits, 256)
+    got_q, got_s = _quantize_on_gpu(torch, z, dtype, x16, bits)
+    assert np.array_equal(got_s[:s.size].view(np.uint32), s.view(np.uint32))
+    assert np.array_equal(got_q[:q.size], q)
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("dtype", [gen.FP16, gen.BF16])
+def test_quantize_where_reciprocal_rounding_would_differ(env, bits, dtype):
+    """A 4M-element input that, as checked here on the CPU, holds elements whose
+    code from rounding x * fl(1/scale) differs from the code of the correctly
+    rounded quotient x / scale: the GPU must still give the quotient's codes."""
+    torch, z = env
+    n = (1 << 22) + 77
+    rng = np.random.default_rng(11 + bits + 3 * dtype)
+    x = (rng.standard_normal(n) * 10.0 ** rng.uniform(-3, 1, n)).astype(np.float32)
+    x16 = oracle.from_float(dtype, x)
+    q, s = oracle.quantize_16(dtype, x16, bits, 256)
+    xf = oracle.to_float(dtype, x16).astype(np.float32)
+    sc = np.repeat(s, 256)[:n]
+    live = sc != 0
+    with np.errstate(all="ignore"):
+        t = xf * (np.float32(1) / sc)
+        y = xf / sc
+    qmax = 127 if bits == 8 else 7
+    differ = (np.clip(np.rint(t), -qmax, qmax) != np.clip(np.rint(y), -qmax, qmax)) & live
+    assert np.count_nonzero(differ) >= 10
+    got_q, got_s = _quantize_on_gpu(torch, z, dtype, x16, bits)
+    assert np.array_equal(got_s[:s.size].view(np.uint32), s.view(np.uint32))
+    assert np.array_equal(got_q[:q.size], q)
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("dtype", [gen.FP16, gen.BF16])
+def test_quantize_weight_like_blocks_near_half_integers(env, bits, dtype):
+    """Weights like the ZeRO-3 workload's (16-bit N(0, 0.02)): with short
+    mantissas, x / scale lands within 2^-14 of a half-integer for about one
+    element in 300 (bf16) or 2500 (fp16), as counted here on the CPU; each of
+    those codes must still be the correctly rounded quotient's."""
+    torch, z = env
+    n = (1 << 21) + 40
+    x16 = gen.s16(5, gen.STREAM_SHARD, 0, 1, n, 0.02, 1.0, dtype)
+    q, s = oracle.quantize_16(dtype, x16, bits, 256)
+    xf = oracle.to_float(dtype, x16).astype(np.float32)
+    sc = np.repeat(s, 256)[:n]
+    with np.errstate(all="ignore"):
+        y = xf / sc
+    near = np.abs(np.abs(y - np.trunc(y)) - 0.5) < 2.0 ** -14
+    assert np.count_nonzero(near) >= (2000 if dtype == gen.BF16 else 200)
+    got_q, got_s = _quantize_on_gpu(torch, z, dtype, x16, bits)
+    assert np.array_equal(got_s[:s.size].view(np.uint32), s.view(np.uint32))
+    assert np.array_equal(got_q[:q.size], q)
+
+
+def _ragged_units():
+    """Units whose lengths leave every rank's slice, and the last rank's valid
+    part, off any multiple of 8; several CTAs per slice."""
+    import dataclasses
+    return dataclasses.replace(W.llama3_8b(), name="ragged",
+                               shapes=[(100003,), (70,), (4095, 1001), (13,), (2,)],
+                               units=[0, 0, 1, 2, 2], nd=5)
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+@pytest.mark.parametrize("model", ["llama-L2h256", "ragged"])
+def test_quantized_unit_gather_bitwise(env, bits, model):
+    torch, z = env
+    w = (W.scaled_llama(2, 256, 512, 8, 2, 1000, 16, W.llama3_8b()) if model == "llama-L2h256"
+         else _ragged_units())
     hp = z.hparams()
     plan = z.zero_plan_create(w.psi, w.nd, 3, w.dtype, w.shapes, hp, units=w.units)
     try:

@@ -38,68 +38,237 @@ static __device__ __forceinline__ int32_t quant1(float x, float scale, float qma
     return c > m ? m : (c < -m ? -m : c);
 }
 
-// One warp per quantization block; lane l takes elements 8l .. 8l+7 of it.
-template <int DT, int BITS>
-__global__ void __launch_bounds__(ZERO_THREADS) k_quantize(const uint16_t* __restrict__ x,
-                                                           int64_t n, uint8_t* __restrict__ codes,
-                                                           float* __restrict__ scales)
+// The 16 bytes x[e .. e+8) when all eight lie below n (else zeros: the widening
+// step then reads the tail element by element).
+static __device__ __forceinline__ uint4 load8_raw(const uint16_t* __restrict__ x, int64_t n, int64_t e)
 {
-    const int lane = threadIdx.x & 31;
-    const int64_t blk = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t e0 = blk * ZERO_QBLOCK + lane * 8;
-    if (blk * ZERO_QBLOCK >= n) return;                      // whole warp out of range
-    float v[8];
-    if (e0 + 8 <= n) {
-        const uint4 q = __ldcs(reinterpret_cast<const uint4*>(x + e0));
+    return e + 8 <= n ? __ldcs(reinterpret_cast<const uint4*>(x + e)) : make_uint4(0, 0, 0, 0);
+}
+
+// Eight elements x[e .. e+8) widened to fp32 from their raw 16 bytes q; elements
+// at or past n read as 0.
+template <int DT>
+static __device__ __forceinline__ void widen8(uint4 q, const uint16_t* __restrict__ x, int64_t n,
+                                              int64_t e, float* v)
+{
+    if (e + 8 <= n) {
         widen2<DT>(q.x, v[0], v[1]);
         widen2<DT>(q.y, v[2], v[3]);
         widen2<DT>(q.z, v[4], v[5]);
         widen2<DT>(q.w, v[6], v[7]);
     } else {
 #pragma unroll
-        for (int e = 0; e < 8; e++) v[e] = e0 + e < n ? widen1<DT>(x[e0 + e]) : 0.0f;
+        for (int i = 0; i < 8; i++) v[i] = e + i < n ? widen1<DT>(x[e + i]) : 0.0f;
     }
-    float amax = 0.0f;
-#pragma unroll
-    for (int e = 0; e < 8; e++) amax = fmaxf(amax, fabsf(v[e]));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+}
+
+// Adding 1.5 * 2^23 to a float t with |t| <= 2^22 rounds it to an integer (nearest,
+// ties to even) and leaves that integer, two's complement, in the low mantissa
+// bits of the sum; the low 8 (or 4) bits of the sum are then the code's byte
+// (nibble).
+#define ZERO_RND 12582912.0f
+
+// Two fp32 values as one packed pair, and the sm_100+ packed arithmetic on pairs
+// (each lane rounded to nearest-even exactly as the scalar operation).
+typedef unsigned long long f32x2_t;
+static __device__ __forceinline__ f32x2_t pack2(float a, float b)
+{
+    f32x2_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+static __device__ __forceinline__ void unpack2(f32x2_t r, float& a, float& b)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+static __device__ __forceinline__ f32x2_t mul2(f32x2_t a, f32x2_t b)
+{
+    f32x2_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+static __device__ __forceinline__ f32x2_t add2(f32x2_t a, f32x2_t b)
+{
+    f32x2_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+static __device__ __forceinline__ f32x2_t sub2(f32x2_t a, f32x2_t b)
+{
+    f32x2_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+// max that returns NaN when either input is NaN
+static __device__ __forceinline__ float max_nan(float a, float b)
+{
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+// t = fl(v * r) rounded to an integer by adding 1.5 * 2^23 (u holds the sum);
+// true when t lies within 2^-14 of a half-integer, or is NaN.
+static __device__ __forceinline__ bool near_half(float v, float r, float* u)
+{
+    const float t = __fmul_rn(v, r);
+    *u = __fadd_rn(t, ZERO_RND);
+    return !(fabsf(__fsub_rn(t, __fsub_rn(*u, ZERO_RND))) <= 0.5f - 0x1p-14f);
+}
+
+// The codes of 16 elements of one block: each is the integer nearest to
+// fl(v / scale) (ties to even), clamped to [-qmax, qmax]; returned as words whose
+// low bits hold the two's-complement code.
+//
+// Fast path, for a scale in the normal range, without a division per element:
+// r = 1 / scale to within 2^-23 relative (the hardware approximation refined by
+// one Newton-Raphson step), t = fl(v * r).  Since |v| <= max|x| and
+// scale = fl(max|x| / qmax), |v / scale| <= qmax (1 + 2^-23), so t is within 2^-16
+// of v / scale and within 2^-15 of fl(v / scale).  Rounding t (by adding
+// 1.5 * 2^23) therefore gives the code unless t lies within 2^-14 of a
+// half-integer, and it never passes qmax (|t| < qmax + 2^-15), so no clamp is
+// needed.  Those elements, and NaN, take the exact quotient instead.  With 16-bit
+// weights they are not rare (about one in 300 for bf16, one in 2500 for fp16):
+// v / scale is then close to qmax m_v / m_max 2^k for the short mantissas of v and
+// max|x|, which often falls next to a half-integer.
+template <int BITS>
+static __device__ __forceinline__ void codes16(const float* v, float scale, uint32_t* c)
+{
     const float qmax = QMax<BITS>::v;
-    const float scale = __fdiv_rn(amax, qmax);
-    if (lane == 0) scales[blk] = scale;
-    int32_t c[8];
+    if (!(scale >= 0x1p-126f && scale <= 0x1p126f)) {
 #pragma unroll
-    for (int e = 0; e < 8; e++) c[e] = quant1(v[e], scale, qmax);
-    if (BITS == 8) {
-        uint32_t lo = 0, hi = 0;
+        for (int i = 0; i < 16; i++) c[i] = (uint32_t)quant1(v[i], scale, qmax);
+        return;
+    }
+    float r0;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r0) : "f"(scale));
+    const float r = __fmaf_rn(__fmaf_rn(-scale, r0, 1.0f), r0, r0);
+    const f32x2_t r2 = pack2(r, r), rnd2 = pack2(ZERO_RND, ZERO_RND);
+    float dmax = 0.0f;
 #pragma unroll
-        for (int e = 0; e < 4; e++) {
-            lo |= (uint32_t)(uint8_t)(int8_t)c[e] << (8 * e);
-            hi |= (uint32_t)(uint8_t)(int8_t)c[4 + e] << (8 * e);
-        }
-        if (e0 + 8 <= n) {
-            *reinterpret_cast<uint2*>(codes + e0) = make_uint2(lo, hi);
-        } else {
-            for (int e = 0; e < 8 && e0 + e < n; e++) codes[e0 + e] = (uint8_t)(int8_t)c[e];
-        }
-    } else {
-        uint32_t w = 0;
+    for (int i = 0; i < 16; i += 2) {                 // near_half, two lanes at a time
+        const f32x2_t t = mul2(pack2(v[i], v[i + 1]), r2);
+        const f32x2_t u = add2(t, rnd2);
+        float d0, d1, u0, u1;
+        unpack2(sub2(t, sub2(u, rnd2)), d0, d1);
+        dmax = max_nan(dmax, fabsf(d0));
+        dmax = max_nan(dmax, fabsf(d1));
+        unpack2(u, u0, u1);
+        c[i] = __float_as_uint(u0);
+        c[i + 1] = __float_as_uint(u1);
+    }
+    if (!(dmax <= 0.5f - 0x1p-14f)) {
 #pragma unroll
-        for (int e = 0; e < 8; e++) w |= (uint32_t)(c[e] & 0xF) << (4 * e);
-        if (e0 + 8 <= n) {
-            *reinterpret_cast<uint32_t*>(codes + e0 / 2) = w;
-        } else {
-            for (int b = 0; 2 * b < 8 && e0 + 2 * b < n; b++)       // odd tail: high nibble 0
-                codes[e0 / 2 + b] = (uint8_t)((w >> (8 * b)) & (e0 + 2 * b + 1 < n ? 0xFF : 0x0F));
+        for (int i = 0; i < 16; i++) {
+            float u;
+            if (near_half(v[i], r, &u)) c[i] = (uint32_t)quant1(v[i], scale, qmax);
         }
     }
 }
 
-// grid.y = rank k; one thread per 16 bytes of codes: EPT = 16 (bits 8) or 32
-// (bits 4) output elements of rank k's slice, all inside one 256-element scale
-// block (unit offsets are multiples of 64).  The thread whose slot runs past the
-// valid part takes the tail element by element.
-template <int BITS> struct Ept { static constexpr int v = BITS == 8 ? 16 : 32; };
+// Store the codes of elements e .. e+8 (those below n).  4-bit codes: two per
+// byte, the even element in the low nibble; an odd tail leaves the high nibble 0.
+template <int BITS>
+static __device__ __forceinline__ void store8(uint8_t* __restrict__ codes, int64_t n, int64_t e,
+                                              const uint32_t* c)
+{
+    if (BITS == 8) {
+        const uint32_t lo = __byte_perm(__byte_perm(c[0], c[1], 0x0040),
+                                        __byte_perm(c[2], c[3], 0x0040), 0x5410);
+        const uint32_t hi = __byte_perm(__byte_perm(c[4], c[5], 0x0040),
+                                        __byte_perm(c[6], c[7], 0x0040), 0x5410);
+        if (e + 8 <= n) {
+            *reinterpret_cast<uint2*>(codes + e) = make_uint2(lo, hi);
+        } else {
+            for (int i = 0; i < 8 && e + i < n; i++) codes[e + i] = (uint8_t)c[i];
+        }
+    } else {
+        uint32_t w = 0;
+#pragma unroll
+        for (int i = 0; i < 8; i++) w |= (c[i] & 0xFu) << (4 * i);
+        if (e + 8 <= n) {
+            *reinterpret_cast<uint32_t*>(codes + e / 2) = w;
+        } else {
+            for (int b = 0; 2 * b < 8 && e + 2 * b < n; b++)
+                codes[e / 2 + b] = (uint8_t)((w >> (8 * b)) & (e + 2 * b + 1 < n ? 0xFF : 0x0F));
+        }
+    }
+}
+
+// One lane's part of a pair: its 16 elements (chunks at e0 and e0 + 128 of block
+// blk, raw bytes q0 and q1) quantized and stored, and the block's scale from the
+// half-warp's first lane.  FULL: the whole pair lies below n (no bounds checks).
+template <int DT, int BITS, bool FULL>
+static __device__ __forceinline__ void quantize_pair(uint4 q0, uint4 q1, const uint16_t* __restrict__ x,
+                                                     int64_t n, int64_t e0, int64_t blk, int lane,
+                                                     uint8_t* __restrict__ codes,
+                                                     float* __restrict__ scales)
+{
+    constexpr int64_t HALF = ZERO_QBLOCK / 2;
+    float v[16];
+    widen8<DT>(q0, x, FULL ? INT64_MAX : n, e0, v);
+    widen8<DT>(q1, x, FULL ? INT64_MAX : n, e0 + HALF, v + 8);
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; i++) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const float scale = __fdiv_rn(amax, QMax<BITS>::v);
+    if ((lane & 15) == 0 && (FULL || blk * ZERO_QBLOCK < n)) scales[blk] = scale;
+    uint32_t c[16];
+    codes16<BITS>(v, scale, c);
+    if (FULL) {
+        store8<BITS>(codes, INT64_MAX, e0, c);
+        store8<BITS>(codes, INT64_MAX, e0 + HALF, c + 8);
+    } else {
+        if (e0 < n) store8<BITS>(codes, n, e0, c);
+        if (e0 + HALF < n) store8<BITS>(codes, n, e0 + HALF, c + 8);
+    }
+}
+
+// Each warp takes two quantization blocks (a pair) at a time, over a persistent
+// grid: half-warp h takes block 2p + h of pair p, and its lane j (0..15) the
+// 8-element chunks j and j + 16 of that block, so every load and store
+// instruction covers two contiguous runs.  The next pair's 32 bytes per lane are
+// loaded before the current pair is quantized, so loads overlap arithmetic.
+template <int DT, int BITS>
+__global__ void __launch_bounds__(ZERO_THREADS, 3) k_quantize(const uint16_t* __restrict__ x,
+                                                           int64_t n, uint8_t* __restrict__ codes,
+                                                           float* __restrict__ scales)
+{
+    constexpr int64_t PAIR = 2 * ZERO_QBLOCK;
+    const int lane = threadIdx.x & 31;
+    const int64_t npairs = (n + PAIR - 1) / PAIR;
+    const int64_t stride = (int64_t)gridDim.x * (ZERO_THREADS / 32);
+    const int64_t sub = (lane >> 4) * ZERO_QBLOCK + (lane & 15) * 8;   // lane's first element
+    int64_t p = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    uint4 nx0 = make_uint4(0, 0, 0, 0), nx1 = nx0;
+    if (p < npairs) {
+        nx0 = load8_raw(x, n, p * PAIR + sub);
+        nx1 = load8_raw(x, n, p * PAIR + sub + ZERO_QBLOCK / 2);
+    }
+    for (; p < npairs; p += stride) {
+        const uint4 q0 = nx0, q1 = nx1;
+        const int64_t e0 = p * PAIR + sub;
+        if (p + stride < npairs) {                               // prefetch the next pair
+            nx0 = load8_raw(x, n, e0 + stride * PAIR);
+            nx1 = load8_raw(x, n, e0 + stride * PAIR + ZERO_QBLOCK / 2);
+        }
+        if ((p + 1) * PAIR <= n)                                  // warp-uniform
+            quantize_pair<DT, BITS, true>(q0, q1, x, n, e0, 2 * p + (lane >> 4), lane, codes, scales);
+        else
+            quantize_pair<DT, BITS, false>(q0, q1, x, n, e0, 2 * p + (lane >> 4), lane, codes, scales);
+    }
+}
+
+// grid.y = rank k.  A CTA covers QG groups of 8 * ZERO_THREADS consecutive
+// outputs of rank k's slice; in group g thread j takes the 8 outputs starting at
+// 8 j, so one warp store writes 512 contiguous bytes.  8 outputs never straddle a
+// 256-element scale block (unit offsets are multiples of 64).  The thread whose
+// 8 outputs run past the valid part takes them element by element.  QG = 2 at 8
+// bits and 4 at 4 bits: at 4 bits a group loads only 4 bytes of codes, and two
+// groups per thread left too few loads in flight.
+template <int BITS> struct Qg { static constexpr int v = BITS == 8 ? 2 : 4; };
 
 static __device__ __forceinline__ int32_t code_at(const uint8_t* codes, int64_t e, int bits)
 {
@@ -112,45 +281,58 @@ static __device__ __forceinline__ int32_t code_at(const uint8_t* codes, int64_t 
 template <int DT, int BITS>
 __global__ void __launch_bounds__(ZERO_THREADS) k_gather_q(const __grid_constant__ GatherQArgs a)
 {
-    constexpr int EPT = Ept<BITS>::v;
     const int k = blockIdx.y;
     const int64_t base = (int64_t)k * a.slice;
     int64_t valid = a.len - base;
     if (valid > a.slice) valid = a.slice;
     if (valid <= 0) return;
-    const int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t nvec = valid / EPT;
     const uint8_t* codes = a.codes[k];
     const float* scales = a.scales[k];
-    if (w < nvec) {
-        const int64_t e = a.offset + w * EPT;                   // element of rank k's shard
-        const float s = __ldg(scales + e / ZERO_QBLOCK);
-        const uint4 q = __ldcs(reinterpret_cast<const uint4*>(codes + e * BITS / 8));
-        const uint32_t word[4] = {q.x, q.y, q.z, q.w};
-        uint4* dst = reinterpret_cast<uint4*>(a.out + base + w * EPT);
+    constexpr int QG = Qg<BITS>::v;
+    const int64_t j0 = (int64_t)blockIdx.x * (QG * 8 * ZERO_THREADS) + 8 * threadIdx.x;
+    uint32_t word[QG][2];
+    float s[QG];
 #pragma unroll
-        for (int v = 0; v < EPT / 8; v++) {                       // 8 outputs per 16-byte store
+    for (int g = 0; g < QG; g++) {                                 // all loads first
+        const int64_t j = j0 + g * 8 * ZERO_THREADS;
+        if (j + 8 <= valid) {
+            const int64_t e = a.offset + j;                        // element of rank k's shard
+            s[g] = __ldg(scales + e / ZERO_QBLOCK);
+            if (BITS == 8) {
+                const uint2 q = __ldcs(reinterpret_cast<const uint2*>(codes + e));
+                word[g][0] = q.x;
+                word[g][1] = q.y;
+            } else {
+                word[g][0] = __ldcs(reinterpret_cast<const unsigned int*>(codes + e / 2));
+                word[g][1] = 0;
+            }
+        }
+    }
+#pragma unroll
+    for (int g = 0; g < QG; g++) {
+        const int64_t j = j0 + g * 8 * ZERO_THREADS;
+        if (j + 8 <= valid) {
             float f[8];
 #pragma unroll
-            for (int j = 0; j < 8; j++) {
-                const int idx = v * 8 + j;                        // element within the thread
+            for (int i = 0; i < 8; i++) {
                 int32_t c;
                 if (BITS == 8) {
-                    c = (int8_t)(word[idx / 4] >> (8 * (idx % 4)));
+                    c = (int8_t)(word[g][i / 4] >> (8 * (i % 4)));
                 } else {
-                    c = (int32_t)((word[idx / 8] >> (4 * (idx % 8))) & 0xF);
+                    c = (int32_t)((word[g][0] >> (4 * i)) & 0xF);
                     c = c >= 8 ? c - 16 : c;
                 }
-                f[j] = __fmul_rn((float)c, s);
+                f[i] = __fmul_rn((float)c, s[g]);
             }
-            __stcs(dst + v, make_uint4(narrow2<DT>(f[0], f[1]), narrow2<DT>(f[2], f[3]),
-                                       narrow2<DT>(f[4], f[5]), narrow2<DT>(f[6], f[7])));
-        }
-    } else if (w == nvec) {
-        for (int64_t j = nvec * EPT; j < valid; j++) {
-            const int64_t e = a.offset + j;
-            a.out[base + j] = narrow1<DT>(__fmul_rn((float)code_at(codes, e, BITS),
-                                                    scales[e / ZERO_QBLOCK]));
+            __stcs(reinterpret_cast<uint4*>(a.out + base + j),
+                   make_uint4(narrow2<DT>(f[0], f[1]), narrow2<DT>(f[2], f[3]),
+                              narrow2<DT>(f[4], f[5]), narrow2<DT>(f[6], f[7])));
+        } else if (j < valid) {
+            for (int64_t i = j; i < valid; i++) {
+                const int64_t e = a.offset + i;
+                a.out[base + i] = narrow1<DT>(__fmul_rn((float)code_at(codes, e, BITS),
+                                                        scales[e / ZERO_QBLOCK]));
+            }
         }
     }
 }
@@ -183,11 +365,18 @@ extern "C" zero_status_t zero_quantize_shard(zero_dtype_t dtype, const void* sha
     if (!shard || !codes || !scales || !aligned_to(shard, 16) || !aligned_to(codes, 16) ||
         !aligned_to(scales, 4))
         return ZERO_EINVAL;
-    const uint64_t nblk = (n + ZERO_QBLOCK - 1) / ZERO_QBLOCK;
-    const uint64_t warps_per_cta = ZERO_THREADS / 32;
-    const uint64_t grid = (nblk + warps_per_cta - 1) / warps_per_cta;
-    if (grid > 0x7FFFFFFFull) return ZERO_EINVAL;
     const void* fn = dtype == ZERO_FP16 ? quantize_kernel<0>(bits) : quantize_kernel<1>(bits);
+    // persistent grid: every resident CTA, or fewer when there are fewer pairs
+    int dev = 0, sms = 1, occ = 1;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, ZERO_THREADS, 0) != cudaSuccess)
+        return ZERO_ECUDA;
+    const uint64_t pairs = (n + 2 * ZERO_QBLOCK - 1) / (2 * ZERO_QBLOCK);
+    const uint64_t warps_per_cta = ZERO_THREADS / 32;
+    uint64_t grid = (pairs + warps_per_cta - 1) / warps_per_cta;
+    const uint64_t resident = (uint64_t)sms * (uint64_t)(occ > 0 ? occ : 1);
+    if (grid > resident) grid = resident;
     const uint16_t* x = static_cast<const uint16_t*>(shard);
     int64_t n64 = (int64_t)n;
     uint8_t* c = static_cast<uint8_t*>(codes);
@@ -227,8 +416,8 @@ extern "C" zero_status_t zero_gather_layer_q(zero_plan_t plan, int unit, int bit
     a->nd = nd;
     cudaError_t e = cudaSuccess;
     if (len > 0) {
-        const int64_t slots = (int64_t)slice / (bits == 8 ? 16 : 32) + 1;
-        const int64_t bx = (slots + ZERO_THREADS - 1) / ZERO_THREADS;
+        const int64_t per_cta = (int64_t)(bits == 8 ? Qg<8>::v : Qg<4>::v) * 8 * ZERO_THREADS;
+        const int64_t bx = ((int64_t)slice + per_cta - 1) / per_cta;
         const void* fn = plan_dtype(plan) == ZERO_FP16 ? gather_q_kernel<0>(bits)
                                                        : gather_q_kernel<1>(bits);
         void* args[] = {a};
