@@ -246,9 +246,9 @@ def config_of(w, padded):
             "optimizer": (f"{'AdamW' if w.weight_decay else 'Adam'} lr {w.lr:g} betas "
                           f"({w.beta1:g}, {w.beta2:g}) eps {w.eps:g}"
                           + (f" wd {w.weight_decay:g}" if w.weight_decay else "")),
-            "l2": (f"inputs ({(2 * w.nd + 14) * padded / 1e9:.1f} GB resident) vs the 129 MB L2"
+            "l2": (f"inputs ({(2 * w.nd + 14) * padded / 1e9:.2f} GB resident) vs the 129 MB L2"
                    + ("; larger, no flush needed" if (2 * w.nd + 14) * padded > (1 << 30) else
-                      "; smaller than 1 GB: timings include L2 reuse")),
+                      "; L2 flushed between steps (256 MB written, then 256 MB read)")),
             "parallelism": "Nd ranks emulated in one GPU's HBM"}
 
 
@@ -335,19 +335,15 @@ def run_ours(args):
     time.sleep(0.5)
     z.zero_plan_profile(plan, 1)
     launches0 = z.zero_plan_kernel_times(plan)["launches"]
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    small = (2 * w.nd + 14) * padded <= (1 << 30)     # inputs could stay in L2: flush
+    flush = l2_flush(torch, dev) if small else None
     barrier(dev)
     torch.cuda.synchronize(dev)
     t_wall0 = time.time()
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
+    ms_local = _timed_steps(torch, stream, step, args.steps, flush)
     t_wall1 = time.time()
     barrier(dev)
     sampler.mark(t_wall0, t_wall1)
-    ms_local = ev0.elapsed_time(ev1)
     kt = z.zero_plan_kernel_times(plan)
     z.zero_plan_profile(plan, 0)
     clocks = sampler.stop()
@@ -482,9 +478,23 @@ def _plan_for(z, w, units=None):
     return z.zero_plan_create(w.psi, w.nd, w.stage, w.dtype, w.shapes, hp, units=units)
 
 
+def l2_flush(torch, dev):
+    """An L2 flush for small inputs: write a 256 MB buffer (twice the 129 MB L2),
+    then read another one.  The read evicts the written lines, so their write-back
+    happens here, outside the timed step, and the step starts with L2 holding only
+    clean lines of no use to it."""
+    wbuf = torch.empty(1 << 28, dtype=torch.uint8, device=dev)
+    rbuf = torch.ones(1 << 26, dtype=torch.float32, device=dev)
+
+    def flush():
+        wbuf.fill_(1)
+        rbuf.sum()
+    return flush
+
+
 def _timed_steps(torch, stream, step, k, flush=None):
     """Device time of k calls of step(): one event pair around all of them, or,
-    with flush (an L2-sized write between steps), one event pair per step."""
+    with flush (l2_flush) between steps, one event pair per step."""
     if flush is None:
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -517,7 +527,7 @@ def run_sweep(args):
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
     peak, _ = measured_peaks()
-    l2 = torch.empty(1 << 28, dtype=torch.uint8, device=dev)          # 256 MB > L2
+    flush = l2_flush(torch, dev)
     for psi in ([args.psi] if args.psi else W.SWEEP_PSI):
         for nd in ([args.nd] if args.nd else W.SWEEP_ND):
             w = W.sweep(psi, nd)
@@ -546,13 +556,14 @@ def run_sweep(args):
             k = max(args.steps, 200 if small else 20)
             ms = _timed_steps(torch, stream,
                               lambda: z.zero_step(plan, grads, master, m, v, params, None, sp),
-                              k, flush=(lambda: l2.fill_(1)) if small else None) / k
+                              k, flush=flush if small else None) / k
             gbs = (2 * nd + 26) * psi / (ms / 1e3) / 1e9
             line.update({"ms_per_step": ms, "params_per_s": psi / (ms / 1e3),
                          "hbm_gbs_roofline_bytes": gbs, "roofline_bytes_per_elem": 2 * nd + 26,
                          "frac_of_measured_hbm": gbs / peak, "peak_gbs": peak, "steps": k,
                          "warmup": 5, "path": "fused single pass",
-                         "l2": "flushed between steps" if small else "inputs larger than L2"})
+                         "l2": ("flushed between steps (256 MB written, then 256 MB read)"
+                                if small else "inputs larger than L2")})
             print(json.dumps(line), flush=True)
             z.zero_plan_destroy(plan)
             del grads, master, m, v, params

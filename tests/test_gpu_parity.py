@@ -267,3 +267,24 @@ def test_tma_staged_reduce_rejects_unsupported(z):
             z.zero_plan_set_reduce_kernel(plan, 0)
         finally:
             z.zero_plan_destroy(plan)
+
+
+def test_profile_fused_path_has_no_update_pass(z):
+    import torch
+    c = H.Case(shapes=[(100_000,)], nd=4, steps=1)              # no clip, no dynamic scale
+    plan = z.zero_plan_create(c.psi, c.nd, 2, c.dtype, c.shapes, c.hparams(z))
+    try:
+        assert z.zero_plan_path(plan) == z.PATH_FUSED
+        _, padded, _, _ = z.zero_plan_layout(plan)
+        dev = torch.device("cuda", 0)
+        g = torch.zeros((4, padded), dtype=torch.int16, device=dev)
+        f = [torch.zeros(padded, dtype=torch.float32, device=dev) for _ in range(3)]
+        p = torch.zeros(padded, dtype=torch.int16, device=dev)
+        z.zero_plan_profile(plan, 1)
+        for _ in range(10):
+            z.zero_step(plan, g, f[0], f[1], f[2], p, None)
+        t = z.zero_plan_kernel_times(plan)
+        assert t["steps"] == 10 and t["launches"] == 10
+        assert t["reduce_ms"] > 0 and t["update_ms"] == 0.0
+    finally:
+        z.zero_plan_destroy(plan)

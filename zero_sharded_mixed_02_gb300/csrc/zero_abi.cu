@@ -26,6 +26,7 @@ constexpr uint64_t TMA_SMEM_MAX = 196608;      // largest ring of stages a CTA m
 struct ProfileSlot {
     cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
     bool used = false;
+    bool one_kernel = false;        // fused path: the step is the first interval
 };
 
 }  // namespace
@@ -327,7 +328,7 @@ void harvest(zero_plan* p, ProfileSlot& s)
     float a = 0.0f, b = 0.0f;
     if (cudaEventSynchronize(s.ev[2]) == cudaSuccess &&
         cudaEventElapsedTime(&a, s.ev[0], s.ev[1]) == cudaSuccess &&
-        cudaEventElapsedTime(&b, s.ev[1], s.ev[2]) == cudaSuccess) {
+        (s.one_kernel || cudaEventElapsedTime(&b, s.ev[1], s.ev[2]) == cudaSuccess)) {
         p->ms_a += a;
         p->ms_b += b;
         p->prof_steps += 1;
@@ -732,6 +733,7 @@ zero_status_t zero_step(zero_plan_t plan, const void* grads, float* master, floa
     if (slot) {
         if (cudaEventRecord(slot->ev[2], s) != cudaSuccess) return ZERO_ECUDA;
         slot->used = true;
+        slot->one_kernel = !plan->fn_b;
     }
     if (cudaEventRecord(plan->ev_done, s) != cudaSuccess) return ZERO_ECUDA;
     plan->stepped = true;
