@@ -726,7 +726,19 @@ zero_status_t zero_step(zero_plan_t plan, const void* grads, float* master, floa
     plan->launches++;
     if (slot && cudaEventRecord(slot->ev[1], s) != cudaSuccess) return ZERO_ECUDA;
     if (plan->fn_b) {
-        e = cudaLaunchKernel(plan->fn_b, dim3((unsigned)plan->grid_b), dim3(ZERO_THREADS), args, 0, s);
+        // a programmatic dependent of pass 1: scheduled while pass 1 finishes, it
+        // waits (griddepcontrol.wait) before reading what pass 1 wrote
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)plan->grid_b);
+        cfg.blockDim = dim3(ZERO_THREADS);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = s;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelExC(&cfg, plan->fn_b, args);
         if (e != cudaSuccess) return ZERO_ECUDA;
         plan->launches++;
     }

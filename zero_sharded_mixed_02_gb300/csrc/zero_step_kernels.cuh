@@ -145,6 +145,9 @@ template <int DT, int ND, bool WRITE_G>
 __global__ void __launch_bounds__(ZERO_THREADS, 4) k_reduce(const StepArgs a)
 {
     __shared__ RedShared sh;
+    // the update pass may be scheduled now: it loads its state, then waits for
+    // this grid to finish before it reads anything this grid writes
+    asm volatile("griddepcontrol.launch_dependents;");
     const int nd = ND > 0 ? ND : a.nd;
     Unscale un;
     un.init(nd, a.state->sc.loss_scale);
@@ -183,26 +186,36 @@ __global__ void __launch_bounds__(ZERO_THREADS, 4) k_reduce(const StepArgs a)
 // One thread per 4 consecutive elements, one launch-wide block per 1024
 // elements (not a persistent grid: measured faster for this read-write mix).
 // The thread whose 4-element slot runs past n takes the ragged tail alone.
+// Launched as a programmatic dependent of pass 1: master, m, v (and, when
+// recomputing, the 16-bit gradients' rank-order sums) are loaded first, since
+// pass 1 does not write them; griddepcontrol.wait then waits for pass 1 to
+// complete before the step status and the fp32 gradient are read.
 template <int DT, int ND, bool RECOMPUTE>
 __global__ void __launch_bounds__(ZERO_THREADS) k_update(const StepArgs a)
 {
-    const DevStatus st = a.state->st;
-    if (st.skipped || st.err) return;
     const int nd = ND > 0 ? ND : a.nd;
-    const float c = st.clip_coef, bc1 = st.bc1, bc2 = st.bc2;
     const int64_t vi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t nvec = a.n >> 2;
+    float4* pm = reinterpret_cast<float4*>(a.master) + vi;
+    float4* mm = reinterpret_cast<float4*>(a.m) + vi;
+    float4* vv = reinterpret_cast<float4*>(a.v) + vi;
+    float4 p{}, m{}, v{};
+    float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (vi < nvec) {
+        p = __ldcs(pm);
+        m = __ldcs(mm);
+        v = __ldcs(vv);
+        if (RECOMPUTE) fold4<DT, ND>(a.grads, a.rank_stride, vi, nd, s);
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const DevStatus st = a.state->st;
+    if (st.skipped || st.err) return;
+    const float c = st.clip_coef, bc1 = st.bc1, bc2 = st.bc2;
     Unscale un;
     if (RECOMPUTE) un.init(nd, st.used_scale);
     if (vi < nvec) {
-        float4* pm = reinterpret_cast<float4*>(a.master) + vi;
-        float4* mm = reinterpret_cast<float4*>(a.m) + vi;
-        float4* vv = reinterpret_cast<float4*>(a.v) + vi;
-        float4 p = __ldcs(pm), m = __ldcs(mm), v = __ldcs(vv);
         float g[4];
         if (RECOMPUTE) {
-            float s[4];
-            fold4<DT, ND>(a.grads, a.rank_stride, vi, nd, s);
 #pragma unroll
             for (int e = 0; e < 4; e++) g[e] = un(s[e]);
         } else {
@@ -221,12 +234,12 @@ __global__ void __launch_bounds__(ZERO_THREADS) k_update(const StepArgs a)
     } else if (vi == nvec) {
         for (int64_t i = nvec << 2; i < a.n; i++) {
             const float g = RECOMPUTE ? un(fold1<DT>(a.grads, a.rank_stride, i, nd)) : a.g32[i];
-            float p = a.master[i], m = a.m[i], v = a.v[i];
-            adam1(g, c, p, m, v, bc1, bc2, a.k);
-            a.master[i] = p;
-            a.m[i] = m;
-            a.v[i] = v;
-            a.params[i] = narrow1<DT>(p);
+            float pi = a.master[i], mi = a.m[i], vi1 = a.v[i];
+            adam1(g, c, pi, mi, vi1, bc1, bc2, a.k);
+            a.master[i] = pi;
+            a.m[i] = mi;
+            a.v[i] = vi1;
+            a.params[i] = narrow1<DT>(pi);
         }
     }
 }
