@@ -10,6 +10,7 @@
 #include "zero_b200.h"
 #include "zero_launch.h"
 #include "zero_plan_access.h"
+#include "zero_trace.h"
 
 using namespace zero;
 
@@ -588,6 +589,7 @@ void bucket_pointers(const zero_plan* plan, void* workspace, float** g32, double
 zero_status_t zero_step_bucket(zero_plan_t plan, uint64_t bucket, const void* bucket_grads,
                                void* workspace, void* stream)
 {
+    zero::TraceRange trace_("zero_step_bucket");
     if (!plan || plan->bucket_elems == 0 || bucket >= plan->nbuckets) return ZERO_EINVAL;
     if (plan->poisoned) return ZERO_ESTATE;
     if (!bucket_grads || !aligned16(bucket_grads) || !workspace || !aligned16(workspace))
@@ -621,6 +623,7 @@ zero_status_t zero_step_bucket(zero_plan_t plan, uint64_t bucket, const void* bu
 zero_status_t zero_step_apply(zero_plan_t plan, float* master, float* m, float* v, void* params,
                               void* workspace, void* stream)
 {
+    zero::TraceRange trace_("zero_step_apply");
     if (!plan || plan->bucket_elems == 0) return ZERO_EINVAL;
     if (plan->poisoned) return ZERO_ESTATE;
     for (uint8_t seen : plan->bucket_seen)
@@ -695,6 +698,7 @@ zero_status_t zero_plan_set_reduce_kernel(zero_plan_t plan, int kind)
 zero_status_t zero_step(zero_plan_t plan, const void* grads, float* master, float* m, float* v,
                         void* params, void* workspace, void* stream)
 {
+    zero::TraceRange trace_("zero_step");
     if (!plan) return ZERO_EINVAL;
     if (plan->poisoned) return ZERO_ESTATE;
     if (plan->n > 0) {
@@ -783,6 +787,7 @@ zero_status_t zero_step_overflow(zero_plan_t plan, int* overflow)
 zero_status_t zero_gather_layer(zero_plan_t plan, int unit, const void* const* shard_ptrs,
                                 void* out, void* stream)
 {
+    zero::TraceRange trace_("zero_gather_layer");
     if (!plan || plan->stage != 3 || unit < 0 || unit >= (int)plan->unit_len.size())
         return ZERO_EINVAL;
     if (plan->poisoned) return ZERO_ESTATE;

@@ -32,6 +32,7 @@
 
 #include "zero_b200.h"
 #include "zero_plan_access.h"
+#include "zero_trace.h"
 
 #if !defined(__BYTE_ORDER__) || __BYTE_ORDER__ != __ORDER_LITTLE_ENDIAN__
 #error "checkpoint files are little-endian and are written by copying host integers"
@@ -762,6 +763,7 @@ extern "C" zero_status_t zero_checkpoint_save(zero_plan_t plan, const char* dir,
                                               const float* v, const void* params, int flags,
                                               void* stream)
 {
+    zero::TraceRange trace_("zero_checkpoint_save");
     const void* src[NARRAYS] = {master, m, v, params};
     if (!args_ok(plan, dir, rank, src)) return ZERO_EINVAL;
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ZERO_ECUDA;
@@ -783,6 +785,7 @@ extern "C" zero_status_t zero_checkpoint_load(zero_plan_t plan, const char* dir,
                                               float* master, float* m, float* v, void* params,
                                               void* stream)
 {
+    zero::TraceRange trace_("zero_checkpoint_load");
     void* dst[NARRAYS] = {master, m, v, params};
     const void* cdst[NARRAYS] = {master, m, v, params};
     if (!args_ok(plan, dir, rank, cdst)) return ZERO_EINVAL;

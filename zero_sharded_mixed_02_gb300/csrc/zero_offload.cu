@@ -23,6 +23,7 @@
 #include "zero_launch.h"
 #include "zero_plan_access.h"
 #include "zero_step_kernels.cuh"
+#include "zero_trace.h"
 
 namespace zero {
 
@@ -166,6 +167,7 @@ extern "C" zero_status_t zero_offload_step(zero_plan_t plan, const void* grads, 
                                            float* m, float* v, void* params, void* workspace,
                                            int nthreads, void* stream)
 {
+    zero::TraceRange trace_("zero_offload_step");
     if (!plan || zero::plan_stage(plan) > 2) return ZERO_EINVAL;
     if (zero::plan_poisoned(plan)) return ZERO_ESTATE;
     zero::PlanLayout L;

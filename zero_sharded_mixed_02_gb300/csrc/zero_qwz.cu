@@ -13,6 +13,7 @@
 #include "zero_b200.h"
 #include "zero_launch.h"
 #include "zero_plan_access.h"
+#include "zero_trace.h"
 
 namespace zero {
 
@@ -360,6 +361,7 @@ bool aligned_to(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t
 extern "C" zero_status_t zero_quantize_shard(zero_dtype_t dtype, const void* shard, uint64_t n,
                                              int bits, void* codes, float* scales, void* stream)
 {
+    zero::TraceRange trace_("zero_quantize_shard");
     if ((dtype != ZERO_FP16 && dtype != ZERO_BF16) || (bits != 8 && bits != 4)) return ZERO_EINVAL;
     if (n == 0) return ZERO_OK;
     if (!shard || !codes || !scales || !aligned_to(shard, 16) || !aligned_to(codes, 16) ||
@@ -392,6 +394,7 @@ extern "C" zero_status_t zero_gather_layer_q(zero_plan_t plan, int unit, int bit
                                              const float* const* scale_ptrs, void* out,
                                              void* stream)
 {
+    zero::TraceRange trace_("zero_gather_layer_q");
     if (!plan || plan_stage(plan) != 3 || (bits != 8 && bits != 4)) return ZERO_EINVAL;
     if (plan_poisoned(plan)) return ZERO_ESTATE;
     uint64_t len = 0, slice = 0, off = 0;
