@@ -132,6 +132,19 @@ def host_mem_available() -> int:
     return 0
 
 
+def pinning_fits(nbytes: int, device=None, avail=None):
+    """Whether every rank on this node can pin nbytes of host memory at once.
+    MemAvailable must cover LOCAL_WORLD_SIZE such buffers plus 8 GB each; the
+    ranks decide together (one rank short and all skip), so they all take the
+    same path through the collectives that follow.  Returns (fits, avail, need)."""
+    _, _, ws = dist_env()
+    local_ws = int(os.environ.get("LOCAL_WORLD_SIZE", str(ws)))
+    avail = host_mem_available() if avail is None else avail
+    need = local_ws * (nbytes + (8 << 30))
+    short = reduce_scalar(0.0 if avail >= need else 1.0, "max", device)
+    return short == 0.0, avail, need
+
+
 class ClockSampler:
     """nvidia-smi samples (every 200 ms) of the SM clock and throttle reasons."""
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -423,12 +436,12 @@ def e2e_leg(args, z, plan, w, grads, master, m, v, params, work, dev, stream):
     device, runs zero_step and reads the step status back."""
     import torch
     nbytes = grads.numel() * 2
-    avail = host_mem_available()
-    if avail and avail < nbytes + (8 << 30):
+    fits, avail, need = pinning_fits(nbytes, dev)
+    if not fits:
         return {"value": None, "unit": "params/s", "h2d_bytes_per_step": nbytes,
                 "d2h_bytes_per_step": STATUS_BYTES,
-                "skipped": f"host has {avail / 1e9:.0f} GB available, needs {nbytes / 1e9:.0f} GB "
-                           "pinned"}
+                "skipped": f"host has {avail / 1e9:.0f} GB available; pinning every local "
+                           f"rank's gradients needs {need / 1e9:.0f} GB"}
     host = torch.empty(grads.shape, dtype=grads.dtype, pin_memory=True)
     host.copy_(grads)
     sp = stream.cuda_stream

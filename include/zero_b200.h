@@ -95,6 +95,11 @@ typedef struct {
 
 /* ---- plans ------------------------------------------------------------ */
 
+/* Largest psi a plan accepts (2^48 elements): far above any GPU's memory, and
+ * small enough that every element index times nd fits the kernels' 64-bit
+ * arithmetic. */
+#define ZERO_MAX_PSI (1ull << 48)
+
 /* Create a plan for a model of psi parameters made of ntensors tensors whose
  * shapes are given in list order: tensor i has ndims[i] dimensions, taken in
  * order from dims.  psi must equal the sum of the tensor sizes.
@@ -110,8 +115,8 @@ typedef struct {
  *     concatenation of its slice of every unit in unit order.
  * The plan copies everything it needs; dims/ndims/hp may be freed afterwards.
  * Allocates the plan's device block on the current device.
- * Errors: ZERO_EINVAL (bad sizes, psi mismatch, dynamic_scale with bf16,
- * nd or stage out of range), ZERO_ENOMEM, ZERO_ECUDA. */
+ * Errors: ZERO_EINVAL (bad sizes, psi mismatch, psi > ZERO_MAX_PSI,
+ * dynamic_scale with bf16, nd or stage out of range), ZERO_ENOMEM, ZERO_ECUDA. */
 zero_status_t zero_plan_create(uint64_t psi, int nd, int stage, zero_dtype_t dtype,
                                const int64_t* dims, const int* ndims, int ntensors,
                                const zero_hparams_t* hp, zero_plan_t* out);

@@ -105,6 +105,16 @@ def test_invalid_plans_rejected_before_cuda(z, case):
     assert e.value.code == z.ZERO_EINVAL
 
 
+@pytest.mark.parametrize("stage", [1, 3])
+def test_psi_beyond_the_limit_rejected(z, stage):
+    # 2^48 + 1 parameters in two tensors: the sizes add up, the plan is refused
+    # before any device call
+    shapes = [(1 << 24, 1 << 24), (1,)]
+    with pytest.raises(z.ZeroError) as e:
+        z.zero_plan_create((1 << 48) + 1, 4, stage, 1, shapes, z.hparams())
+    assert e.value.code == z.ZERO_EINVAL
+
+
 def test_stage3_units_must_be_contiguous(z):
     shapes = [(4,), (4,), (4,)]
     with pytest.raises(z.ZeroError) as e:

@@ -32,6 +32,37 @@ def _worker(rank, world, port, q):
     dist.destroy_process_group()
 
 
+def _pin_worker(rank, world, port, q):
+    os.environ.update(RANK=str(rank), LOCAL_RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_WORLD_SIZE=str(world), MASTER_ADDR="127.0.0.1",
+                      MASTER_PORT=str(port))
+    sys.path.insert(0, ROOT)
+    import bench
+    import torch.distributed as dist
+    bench.dist_init("gloo")
+    gb = 1 << 30
+    # 2 local ranks x (50 + 8) GB = 116 GB: enough on both ranks, then rank 1 short
+    both = bench.pinning_fits(50 * gb, avail=200 * gb)
+    one_short = bench.pinning_fits(50 * gb, avail=200 * gb if rank == 0 else 100 * gb)
+    q.put((rank, both[0], both[2], one_short[0]))
+    dist.destroy_process_group()
+
+
+def test_host_pinning_decided_for_all_local_ranks():
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = free_port()
+    procs = [ctx.Process(target=_pin_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    assert got == [(0, True, 2 * 58 * (1 << 30), False), (1, True, 2 * 58 * (1 << 30), False)]
+
+
 def test_timing_reductions_over_two_gloo_ranks():
     import torch.multiprocessing as mp
     ctx = mp.get_context("spawn")

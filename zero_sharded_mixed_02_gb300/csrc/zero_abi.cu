@@ -193,7 +193,7 @@ zero_status_t create_impl(uint64_t psi, int nd, int stage, zero_dtype_t dtype,
         if (total > UINT64_MAX - len) return ZERO_EINVAL;
         total += len;
     }
-    if (total != psi) return ZERO_EINVAL;
+    if (total != psi || psi > ZERO_MAX_PSI) return ZERO_EINVAL;
 
     zero_plan* p = new (std::nothrow) zero_plan();
     if (!p) return ZERO_ENOMEM;
