@@ -17,7 +17,9 @@ namespace zero {
 #define ZERO_TMA_TILE 1024            // elements per tile (4 per consumer thread)
 #define ZERO_TMA_MAX_STAGES 8
 #define ZERO_TMA_THREADS 288          // 8 consumer warps + 1 producer warp
+#ifndef ZERO_TMA_WAIT_LIMIT                  // polls before a wait gives up
 #define ZERO_TMA_WAIT_LIMIT (1u << 20)
+#endif
 
 static __device__ __forceinline__ uint32_t smem_u32(const void* p)
 {
