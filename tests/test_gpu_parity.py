@@ -288,3 +288,68 @@ def test_profile_fused_path_has_no_update_pass(z):
         assert t["reduce_ms"] > 0 and t["update_ms"] == 0.0
     finally:
         z.zero_plan_destroy(plan)
+
+
+# ---- the largest rank counts the boundary accepts (nd up to 1024) ----
+@pytest.mark.parametrize("nd", [1000, 1024])
+@pytest.mark.parametrize("mode", ["clip", "fp16-dyn"])
+def test_largest_rank_counts(z, nd, mode):
+    # the generic-nd fold over up to 1024 rank rows; shards of 128 elements
+    shapes = [(70_001,), (13,)]
+    if mode == "clip":
+        c = H.Case(shapes=shapes, nd=nd, steps=2, clip=0.05, weight_decay=0.01)
+    else:
+        c = H.Case(shapes=shapes, nd=nd, steps=3, dtype=gen.FP16, grad_sigma=1e-3,
+                   loss_scale=4096.0, dynamic_scale=1, inf_steps=(2,))
+    gpu, _ = check(z, c, bit_exact=(mode != "clip"), g32=True)
+    if mode != "clip":
+        assert [r["skipped"] for r in gpu.results] == [0, 1, 0]
+
+
+def test_largest_rank_count_stage3_gathers(z):
+    # ZeRO-3 at nd = 1000: rank 0's shard updated, then each unit assembled from
+    # 1000 shards (the gather's per-rank pointer table at its largest use), both
+    # 16-bit and 8-bit quantized
+    import torch
+    nd = 1000
+    c = H.Case(shapes=[(40_000,), (7,), (3_001, 3)], nd=nd, stage=3, units=[0, 0, 1], steps=2,
+               clip=1.0)
+    plans = []
+    gpu = H.run_gpu(z, c, plan_out=plans)
+    plan = plans[0]
+    try:
+        _, total, nunits, _ = z.zero_plan_layout(plan)
+        assert nunits == 2
+        mask = H.stage3_valid_mask(z, plan, nd)
+        ora = H.run_oracle(c, total, total, mask)
+        H.compare_runs(gpu, ora, "stage3 nd=1000")
+        dev = torch.device("cuda", 0)
+        sp = torch.cuda.current_stream().cuda_stream
+        host_shards = [gpu.params]
+        for k in range(1, nd):
+            s = gen.s16(c.seed, gen.STREAM_SHARD, 0, k, total, 0.02, 1.0, c.dtype)
+            s[~H.stage3_valid_mask(z, plan, nd, rank=k)] = 0
+            host_shards.append(s)
+        stacked = torch.from_numpy(np.stack(host_shards).view(np.int16)).to(dev)
+        shards = [stacked[k] for k in range(nd)]
+        qs = [oracle.quantize_16(c.dtype, s, 8, 256) for s in host_shards]
+        codes = torch.from_numpy(np.stack([q for q, _ in qs])).to(dev)
+        scales = torch.from_numpy(np.stack([s for _, s in qs])).to(dev)
+        for u in range(nunits):
+            ln, sl, off = z.zero_plan_unit(plan, u)
+            out = torch.full((ln + 8,), -1, dtype=torch.int16, device=dev)
+            z.zero_gather_layer(plan, u, shards, out, sp)
+            torch.cuda.synchronize()
+            got = out.cpu().numpy().view(np.uint16)
+            want = oracle.gather_unit(nd, ln, sl, [s[off:off + sl] for s in host_shards])
+            assert np.array_equal(got[:ln], want) and np.all(got[ln:] == 0xFFFF)
+            out.fill_(-1)
+            z.zero_gather_layer_q(plan, u, 8, [codes[k] for k in range(nd)],
+                                  [scales[k] for k in range(nd)], out, sp)
+            torch.cuda.synchronize()
+            got = out.cpu().numpy().view(np.uint16)
+            want = oracle.gather_unit_q(c.dtype, nd, ln, sl, off, 8, 256, [q for q, _ in qs],
+                                        [s for _, s in qs])
+            assert np.array_equal(got[:ln], want) and np.all(got[ln:] == 0xFFFF)
+    finally:
+        z.zero_plan_destroy(plan)
