@@ -77,19 +77,24 @@ class Case:
     units: Optional[List[int]] = None
     seed: int = 0
     growth_interval: int = 1000
+    beta1: float = 0.9
+    beta2: float = 0.999
+    eps: float = 1e-8
 
     @property
     def psi(self):
         return int(sum(int(np.prod(s)) for s in self.shapes))
 
     def opt(self):
-        return oracle.Opt(lr=self.lr, weight_decay=self.weight_decay,
+        return oracle.Opt(lr=self.lr, beta1=self.beta1, beta2=self.beta2, eps=self.eps,
+                          weight_decay=self.weight_decay,
                           decoupled_wd=self.decoupled_wd, clip_norm=self.clip,
                           dynamic_scale=self.dynamic_scale, backoff=0.5,
                           growth_interval=self.growth_interval)
 
     def hparams(self, z):
-        return z.hparams(lr=self.lr, weight_decay=self.weight_decay,
+        return z.hparams(lr=self.lr, beta1=self.beta1, beta2=self.beta2, eps=self.eps,
+                         weight_decay=self.weight_decay,
                          decoupled_wd=self.decoupled_wd, clip_norm=self.clip,
                          loss_scale=self.loss_scale, dynamic_scale=self.dynamic_scale,
                          backoff=0.5, growth_interval=self.growth_interval)

@@ -353,3 +353,31 @@ def test_largest_rank_count_stage3_gathers(z):
             assert np.array_equal(got[:ln], want) and np.all(got[ln:] == 0xFFFF)
     finally:
         z.zero_plan_destroy(plan)
+
+
+# ---- degenerate settings of the method ----
+DEGENERATE = {
+    "lr-zero": dict(lr=0.0, clip=1.0),                  # master unchanged; m and v still advance
+    "beta1-zero": dict(beta1=0.0, clip=1.0),            # m is the (clipped) gradient itself
+    "beta2-zero": dict(beta2=0.0),                      # v is the squared gradient itself
+    "clip-vanishing": dict(clip=1e-30),                 # c ~ 5e-31: the squares of the clipped gradients underflow to 0
+    "l2-decay-clip": dict(weight_decay=0.5, decoupled_wd=0, clip=0.1),
+    "eps-large": dict(eps=1.0, clip=1.0),
+}
+
+
+@pytest.mark.parametrize("name", sorted(DEGENERATE))
+@pytest.mark.parametrize("kernels", [None, 0])
+def test_degenerate_settings(z, name, kernels):
+    # against the oracle; the two-pass kernels and the plan's own choice.  With
+    # the clip on, the state is within tolerance (c may differ in its last bit);
+    # without it, bit for bit.
+    kw = DEGENERATE[name]
+    c = H.Case(shapes=[(50_003,), (5,)], nd=4, steps=3, **kw)
+    gpu, _ = check(z, c, bit_exact=not kw.get("clip"), reduce_kernel=kernels)
+    if name == "lr-zero":
+        master0 = gen.f32(c.seed, gen.STREAM_MASTER, 0, 0, c.psi, 0.02)
+        assert gpu.master.tobytes() == master0.tobytes()
+        assert np.any(gpu.m != 0) and np.any(gpu.v != 0)
+    if name == "clip-vanishing":
+        assert all(r["clip_coef"] < 1e-28 for r in gpu.results)
