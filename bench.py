@@ -499,44 +499,65 @@ def e2e_leg(args, z, plan, w, grads, master, m, v, params, work, dev, stream):
     host.copy_(grads)
     sp = stream.cuda_stream
     K = max(3, min(args.steps, args.e2e_steps))
-    # the host->device copy is split by rank rows over several copy streams, which
-    # the step's stream then waits for
-    ns = max(1, min(args.e2e_streams, grads.shape[0]))
-    copy_streams = [torch.cuda.Stream(dev) for _ in range(ns)]
-    rows = [(grads.shape[0] * k // ns, grads.shape[0] * (k + 1) // ns) for k in range(ns)]
+    # Two device gradient buffers when they fit: step k+1's gradients are copied on
+    # a copy stream while step k runs, and a buffer is refilled only after the step
+    # that read it has finished.  Every step still copies its own 49.8 GB and reads
+    # its status back; with one buffer the copies and steps alternate.
+    two = torch.cuda.mem_get_info(dev)[0] > nbytes + (4 << 30)
+    bufs = [grads, torch.empty_like(grads)] if two else [grads]
+    cs = torch.cuda.Stream(dev)
+    consumed = [None] * len(bufs)
+    copied = [None] * len(bufs)
 
-    def h2d():
-        ready = torch.cuda.Event()
-        ready.record(stream)
-        for cs, (a, b) in zip(copy_streams, rows):
-            cs.wait_event(ready)
-            with torch.cuda.stream(cs):
-                for r in range(a, b):                         # one copy per rank row
-                    grads[r].copy_(host[r], non_blocking=True)
-            done = torch.cuda.Event()
-            done.record(cs)
-            stream.wait_event(done)
+    def h2d(k):
+        i = k % len(bufs)
+        if consumed[i] is None:                     # first use: after the queued work
+            ev = torch.cuda.Event()
+            ev.record(stream)
+            cs.wait_event(ev)
+        else:
+            cs.wait_event(consumed[i])
+        with torch.cuda.stream(cs):
+            for r in range(bufs[i].shape[0]):       # one copy per rank row
+                bufs[i][r].copy_(host[r], non_blocking=True)
+        copied[i] = torch.cuda.Event()
+        copied[i].record(cs)
 
-    for _ in range(2):
-        h2d()
-        z.zero_step(plan, grads, master, m, v, params, work, sp)
+    def step(k):
+        i = k % len(bufs)
+        stream.wait_event(copied[i])
+        z.zero_step(plan, bufs[i], master, m, v, params, work, sp)
+        consumed[i] = torch.cuda.Event()
+        consumed[i].record(stream)
         z.zero_step_result(plan)
+
+    def run(n):
+        h2d(0)
+        for k in range(n):
+            if len(bufs) > 1 and k + 1 < n:
+                h2d(k + 1)
+            step(k)
+            if len(bufs) == 1 and k + 1 < n:
+                h2d(k + 1)
+
+    run(2)
     barrier(dev)
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
-    for _ in range(K):
-        h2d()
-        z.zero_step(plan, grads, master, m, v, params, work, sp)
-        z.zero_step_result(plan)
+    run(K)
     torch.cuda.synchronize(dev)
     dt = reduce_scalar(time.perf_counter() - t0, "max", dev)
     _, _, ws = dist_env()
     del host
     if pinned is not None:
         pinned.release()
+    del bufs
     return {"value": w.psi * K * ws / dt, "unit": "params/s", "h2d_bytes_per_step": nbytes,
             "d2h_bytes_per_step": STATUS_BYTES, "steps": K, "ms_per_step": dt / K * 1e3,
-            "h2d_gbs": nbytes / (dt / K) / 1e9, "copy_streams": ns, "host_memory": host_kind}
+            "h2d_gbs": nbytes / (dt / K) / 1e9, "device_buffers": 2 if two else 1,
+            "overlap": ("step k+1's copy runs during step k" if two else
+                        "copies and steps alternate"),
+            "host_memory": host_kind}
 
 
 # ------------------------------------------------------------ sweep and ZeRO-3
@@ -1059,8 +1080,6 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
-    ap.add_argument("--e2e-streams", type=int, default=1,
-                    help="copy streams the host->device gradient copy is split over")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=1 << 23)
     ap.add_argument("--ref-sample", type=int, default=1 << 21)
