@@ -52,6 +52,9 @@ extern "C" {
 
 typedef struct zero_plan* zero_plan_t;
 
+/* Every entry point reports through its return value and never throws: a C++
+ * exception inside the library (a host allocation or a worker thread that
+ * cannot be had) comes back as ZERO_ENOMEM, or ZERO_EIO inside checkpoint IO. */
 typedef enum {
     ZERO_OK       = 0,
     ZERO_EINVAL   = 1,   /* an argument is out of range, null or misaligned   */

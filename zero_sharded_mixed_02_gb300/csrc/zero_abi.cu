@@ -499,7 +499,11 @@ zero_status_t zero_plan_create(uint64_t psi, int nd, int stage, zero_dtype_t dty
                                const int64_t* dims, const int* ndims, int ntensors,
                                const zero_hparams_t* hp, zero_plan_t* out)
 {
-    return create_impl(psi, nd, stage, dtype, dims, ndims, ntensors, nullptr, hp, out);
+    try {
+        return create_impl(psi, nd, stage, dtype, dims, ndims, ntensors, nullptr, hp, out);
+    } catch (...) {                             // host allocation failed: nothing escapes the ABI
+        return ZERO_ENOMEM;
+    }
 }
 
 zero_status_t zero_plan_create_units(uint64_t psi, int nd, int stage, zero_dtype_t dtype,
@@ -508,7 +512,11 @@ zero_status_t zero_plan_create_units(uint64_t psi, int nd, int stage, zero_dtype
                                      zero_plan_t* out)
 {
     if (stage == 3 && ntensors > 0 && !unit_of_tensor) return ZERO_EINVAL;
-    return create_impl(psi, nd, stage, dtype, dims, ndims, ntensors, unit_of_tensor, hp, out);
+    try {
+        return create_impl(psi, nd, stage, dtype, dims, ndims, ntensors, unit_of_tensor, hp, out);
+    } catch (...) {
+        return ZERO_ENOMEM;
+    }
 }
 
 zero_status_t zero_plan_destroy(zero_plan_t plan)
@@ -565,7 +573,12 @@ zero_status_t zero_plan_set_bucket(zero_plan_t plan, uint64_t bucket_elems,
     plan->nbuckets = nb;
     plan->bucket_ws = round_up(plan->n * sizeof(float), 256) + round_up(nb * sizeof(double), 256) +
                       round_up(nb * sizeof(int32_t), 256);
-    plan->bucket_seen.assign((size_t)nb, 0);
+    try {
+        plan->bucket_seen.assign((size_t)nb, 0);
+    } catch (...) {
+        plan->bucket_elems = plan->nbuckets = plan->bucket_ws = 0;
+        return ZERO_ENOMEM;
+    }
     plan->fn_bucket_reduce = red;
     plan->fn_bucket_final = fin;
     plan->fn_bucket_update = upd;
@@ -884,10 +897,20 @@ zero_status_t zero_plan_profile(zero_plan_t plan, int enable)
         return ZERO_OK;
     }
     if (plan->ring.empty()) {
-        plan->ring.resize(PROFILE_RING);
+        try {
+            plan->ring.resize(PROFILE_RING);
+        } catch (...) {
+            return ZERO_ENOMEM;
+        }
         for (auto& s : plan->ring)
             for (auto& e : s.ev)
-                if (cudaEventCreate(&e) != cudaSuccess) return ZERO_ECUDA;
+                if (cudaEventCreate(&e) != cudaSuccess) {   // undo: no half-made ring is kept
+                    for (auto& s2 : plan->ring)
+                        for (auto& e2 : s2.ev)
+                            if (e2) cudaEventDestroy(e2);
+                    plan->ring.clear();
+                    return ZERO_ECUDA;
+                }
     }
     for (auto& s : plan->ring) {
         if (s.used) cudaEventSynchronize(s.ev[2]);

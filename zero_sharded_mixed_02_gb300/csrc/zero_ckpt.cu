@@ -773,6 +773,8 @@ extern "C" zero_status_t zero_checkpoint_save(zero_plan_t plan, const char* dir,
         st = save_impl(plan, dir, rank, src, flags, files);
     } catch (const std::bad_alloc&) {
         st = ZERO_ENOMEM;
+    } catch (...) {                             // nothing escapes the ABI
+        st = ZERO_EIO;
     }
     for (ShardOut& F : files) {                     // on failure: no file under a final name
         if (F.fd >= 0) close(F.fd);
@@ -796,6 +798,8 @@ extern "C" zero_status_t zero_checkpoint_load(zero_plan_t plan, const char* dir,
         st = load_impl(plan, dir, rank, dst, shards);
     } catch (const std::bad_alloc&) {
         st = ZERO_ENOMEM;
+    } catch (...) {
+        st = ZERO_EIO;
     }
     for (ShardIn& S : shards)
         if (S.fd >= 0) close(S.fd);

@@ -279,7 +279,7 @@ extern "C" zero_status_t zero_cpu_adam(const void* grads16, zero_dtype_t dtype, 
             const int64_t hi = std::min<int64_t>((int64_t)n, groups * (i + 1) / size * 64);
             if (hi > lo) zero::host_adam_range(a, g + lo, master + lo, m + lo, v + lo, out + lo, hi - lo);
         });
-    } catch (const std::bad_alloc&) {
+    } catch (...) {                             // allocation or thread start: nothing escapes
         return ZERO_ENOMEM;
     }
     return ZERO_OK;

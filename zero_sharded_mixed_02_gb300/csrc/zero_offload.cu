@@ -206,7 +206,7 @@ extern "C" zero_status_t zero_offload_step(zero_plan_t plan, const void* grads, 
     try {
         return host_pipeline(plan, a, L.psi, static_cast<const uint16_t*>(workspace), master, m, v,
                              static_cast<uint16_t*>(params), nthreads);
-    } catch (const std::bad_alloc&) {
+    } catch (...) {                             // host allocation or threads: nothing escapes
         return ZERO_ENOMEM;
     }
 }
