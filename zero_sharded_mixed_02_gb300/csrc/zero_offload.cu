@@ -98,6 +98,10 @@ struct Copies {
     cudaEvent_t ev_d[2] = {nullptr, nullptr}, ev_h[2] = {nullptr, nullptr};
     ~Copies()
     {
+        // an early return may leave copies in flight into the plan's staging: let
+        // them finish before the next call can reuse it
+        if (d2h) cudaStreamSynchronize(d2h);
+        if (h2d) cudaStreamSynchronize(h2d);
         for (cudaEvent_t e : ev_d)
             if (e) cudaEventDestroy(e);
         for (cudaEvent_t e : ev_h)
