@@ -381,3 +381,23 @@ def test_degenerate_settings(z, name, kernels):
         assert np.any(gpu.m != 0) and np.any(gpu.v != 0)
     if name == "clip-vanishing":
         assert all(r["clip_coef"] < 1e-28 for r in gpu.results)
+
+
+@pytest.mark.parametrize("nd", [3, 16])
+@pytest.mark.parametrize("mode", ["fused", "clip", "fp16-dyn"])
+def test_stage3_modes(z, nd, mode):
+    # ZeRO-3 (one rank's shard resident, its nd contributions) on every kernel path,
+    # with ragged units; state against the oracle, skips and scale schedule exact
+    shapes, units = [(30_011,), (7,), (1_000, 13), (5,)], [0, 0, 1, 2]
+    if mode == "fused":
+        c = H.Case(shapes=shapes, nd=nd, stage=3, units=units, steps=3, weight_decay=0.01)
+    elif mode == "clip":
+        c = H.Case(shapes=shapes, nd=nd, stage=3, units=units, steps=3, clip=0.05,
+                   weight_decay=0.01, decoupled_wd=0)
+    else:
+        c = H.Case(shapes=shapes, nd=nd, stage=3, units=units, steps=4, dtype=gen.FP16,
+                   grad_sigma=1e-3, loss_scale=4096.0, dynamic_scale=1, inf_steps=(2,),
+                   growth_interval=2)
+    gpu, _ = check(z, c, bit_exact=(mode != "clip"))
+    if mode == "fp16-dyn":
+        assert [r["skipped"] for r in gpu.results] == [0, 1, 0, 0]
