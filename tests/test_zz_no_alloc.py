@@ -1,6 +1,7 @@
 """zero_grad_norm_noalloc -- the gradient norm and overflow flag for callers that
-may not allocate device memory -- against what zero_step reports on the same
-gradients, for two calls in a row (the second reuses the library's fixed
+may not allocate device memory -- against the oracle (its rank-order reduce and
+its binary64 sum of squares, taken on the same gradients) and against what
+zero_step reports, for two calls in a row (the second reuses the library's fixed
 scratch array, with a different size and different data).
 
 This file is collected last so a stop-at-first-failure run has already run every
@@ -10,6 +11,7 @@ import pytest
 
 import gen
 import harness as H
+import oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -55,6 +57,13 @@ def noalloc(torch, z, grads_host, nd, psi, rank_stride, dtype, scale):
     return float(norm.item()), int(ovf.item())
 
 
+def oracle_norm(g, nd, psi, dtype, scale):
+    """The oracle's norm and flag: its reduce of the first psi elements of every
+    rank's row, then the square root of its binary64 sum of squares."""
+    gr, ovf = oracle.reduce(nd, dtype, np.ascontiguousarray(g[:, :psi]), loss_scale=scale)
+    return float(np.sqrt(oracle.sumsq(gr))), int(ovf)
+
+
 def grads(nd, psi, dtype, sigma, scale, step, inf=False):
     padded = (-(-psi // nd) + 63) // 64 * 64 * nd
     g = gen.ranks_16(0, gen.STREAM_GRAD, step, nd, psi, sigma, scale, dtype, rank_stride=padded)
@@ -74,7 +83,9 @@ def test_two_calls_in_a_row_match_zero_step(env, nd, dtype, sigma, scale, sizes)
         g, padded = grads(nd, psi, dtype, sigma, scale, step=call)
         want_norm, want_ovf = existing_entry_point(torch, z, g, nd, psi, dtype, scale)
         got_norm, got_ovf = noalloc(torch, z, g, nd, psi, padded, dtype, scale)
-        assert got_ovf == want_ovf == 0
+        ora_norm, ora_ovf = oracle_norm(g, nd, psi, dtype, scale)
+        assert got_ovf == ora_ovf == want_ovf == 0
+        assert abs(got_norm - ora_norm) <= H.REL_NORM * ora_norm, (call, got_norm, ora_norm)
         assert abs(got_norm - want_norm) <= H.REL_NORM * want_norm, (call, got_norm, want_norm)
 
 
@@ -84,12 +95,17 @@ def test_overflow_flag_then_clean_call(env):
     g, padded = grads(nd, psi, gen.FP16, 1e-3, 1024.0, step=3, inf=True)
     want_norm, want_ovf = existing_entry_point(torch, z, g, nd, psi, gen.FP16, 1024.0)
     got_norm, got_ovf = noalloc(torch, z, g, nd, psi, padded, gen.FP16, 1024.0)
-    assert got_ovf == want_ovf == 1
-    assert not np.isfinite(got_norm) and not np.isfinite(want_norm)
+    ora_norm, ora_ovf = oracle_norm(g, nd, psi, gen.FP16, 1024.0)
+    assert got_ovf == ora_ovf == want_ovf == 1
+    assert not np.isfinite(got_norm) and not np.isfinite(ora_norm)
+    assert not np.isfinite(want_norm)
     g, padded = grads(nd, psi, gen.FP16, 1e-3, 1024.0, step=4)        # the flag must not stick
     want_norm, _ = existing_entry_point(torch, z, g, nd, psi, gen.FP16, 1024.0)
     got_norm, got_ovf = noalloc(torch, z, g, nd, psi, padded, gen.FP16, 1024.0)
-    assert got_ovf == 0 and abs(got_norm - want_norm) <= H.REL_NORM * want_norm
+    ora_norm, ora_ovf = oracle_norm(g, nd, psi, gen.FP16, 1024.0)
+    assert got_ovf == ora_ovf == 0
+    assert abs(got_norm - ora_norm) <= H.REL_NORM * ora_norm
+    assert abs(got_norm - want_norm) <= H.REL_NORM * want_norm
 
 
 def test_sizes_beyond_the_scratch_are_rejected(env):

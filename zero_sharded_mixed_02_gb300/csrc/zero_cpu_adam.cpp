@@ -32,6 +32,16 @@ inline float u2f(uint32_t u)
     return f;
 }
 
+// The two binary16 conversions below follow the published, public-domain
+// bit-manipulation method for half-precision conversion described by Fabian
+// "ryg" Giesen (his "half to float" / "float to half" routines and the write-up
+// accompanying them, 2012-2013): widen by moving the exponent and fraction
+// into place and rescaling with one exact multiplication; narrow by adding the
+// exponent rebias and 0xFFF plus the kept bit's parity (round to nearest even),
+// with subnormal results produced by the FPU through an added 0.5.  The code
+// here is written from that description and tested exhaustively against the
+// oracle's own conversions.
+//
 // binary16 -> binary32, exact.  The half's exponent and fraction bits moved up
 // by 13 places, read as a binary32, are the half's value times 2^-112, for
 // normal and subnormal halves alike (a half subnormal m 2^-24 becomes the

@@ -96,22 +96,69 @@ k_norm_noalloc(const uint16_t* __restrict__ grads, int nd, int64_t n, int64_t ra
     }
 }
 
-// Device address of the scratch array, looked up once per device.
+// Device address of the scratch array, looked up once per device context.
+// The address belongs to the module loaded in that context: after the device's
+// primary context is destroyed and created again (cudaDeviceReset), the module
+// is loaded anew and the array may sit elsewhere, so each entry remembers the
+// driver's unique id of the context it was looked up in and is refreshed when
+// the current context's id differs.
 constexpr int MAX_CACHED_DEVICES = 64;
+struct ScratchEntry {
+    unsigned long long ctx_id = 0;     // 0: unknown (no driver query available)
+    void* addr = nullptr;
+};
 std::mutex g_setup_mutex;
-void* g_scratch_addr[MAX_CACHED_DEVICES] = {};
+ScratchEntry g_scratch[MAX_CACHED_DEVICES];
+
+using CtxGetCurrentFn = int (*)(void**);
+using CtxGetIdFn = int (*)(void*, unsigned long long*);
+CtxGetCurrentFn g_ctx_current = nullptr;
+CtxGetIdFn g_ctx_id = nullptr;
+bool g_ctx_fns_looked_up = false;
+
+// Unique id of the calling thread's current context, 0 when there is none or
+// the driver offers no query (caller holds g_setup_mutex).
+unsigned long long current_ctx_id()
+{
+    if (!g_ctx_fns_looked_up) {
+        g_ctx_fns_looked_up = true;
+        void* f1 = nullptr;
+        void* f2 = nullptr;
+        cudaDriverEntryPointQueryResult q1, q2;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault,
+                                             &q1) == cudaSuccess &&
+            q1 == cudaDriverEntryPointSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) ==
+                cudaSuccess &&
+            q2 == cudaDriverEntryPointSuccess) {
+            g_ctx_current = reinterpret_cast<CtxGetCurrentFn>(f1);
+            g_ctx_id = reinterpret_cast<CtxGetIdFn>(f2);
+        }
+    }
+    if (!g_ctx_current || !g_ctx_id) return 0;
+    void* ctx = nullptr;
+    unsigned long long id = 0;
+    if (g_ctx_current(&ctx) != 0 || ctx == nullptr) return 0;
+    if (g_ctx_id(ctx, &id) != 0) return 0;
+    return id;
+}
 
 cudaError_t scratch_address(int device, unsigned char** out)
 {
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (device >= 0 && device < MAX_CACHED_DEVICES && g_scratch_addr[device]) {
-        *out = static_cast<unsigned char*>(g_scratch_addr[device]);
+    const bool cached = device >= 0 && device < MAX_CACHED_DEVICES;
+    const unsigned long long id = current_ctx_id();
+    if (cached && g_scratch[device].addr && g_scratch[device].ctx_id == id) {
+        *out = static_cast<unsigned char*>(g_scratch[device].addr);
         return cudaSuccess;
     }
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess || p == nullptr) return e != cudaSuccess ? e : cudaErrorInvalidSymbol;
-    if (device >= 0 && device < MAX_CACHED_DEVICES) g_scratch_addr[device] = p;
+    if (cached) {
+        g_scratch[device].ctx_id = current_ctx_id();   // the lookup made the context current
+        g_scratch[device].addr = p;
+    }
     *out = static_cast<unsigned char*>(p);
     return cudaSuccess;
 }

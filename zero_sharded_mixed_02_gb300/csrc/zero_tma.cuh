@@ -6,8 +6,9 @@
 // by transaction count; eight consumer warps fold the staged rows in rank order,
 // release the stage through a second mbarrier, and write the fp32 gradient.
 // Every wait is bounded: after WAIT_LIMIT polls the block raises a shared abort
-// flag and the sticky error bit of the step status, lets its own copies land,
-// and finishes without further work (the host sees ZERO_ETIMEOUT).
+// flag and the sticky error bit of the step status; once every warp has stopped,
+// the producer lets the block's copies still in flight land (again bounded), and
+// the block finishes without further work (the host sees ZERO_ETIMEOUT).
 #pragma once
 
 #include "zero_step_kernels.cuh"
@@ -150,6 +151,7 @@ __global__ void __launch_bounds__(ZERO_TMA_THREADS, 1) k_reduce_tma(const StepAr
     __syncthreads();
     double acc = 0.0;
     int bad = 0;
+    int64_t issued = 0;                                     // tiles the producer issued
     if (warp == 8) {                                        // producer
         if (lane == 0) {
             int64_t j = 0, base = (int64_t)blockIdx.x * ZERO_TMA_TILE;
@@ -171,13 +173,7 @@ __global__ void __launch_bounds__(ZERO_TMA_THREADS, 1) k_reduce_tma(const StepAr
                         bulk_g2s(sb + r * ROW, a.grads + (int64_t)r * a.rank_stride + base, ROW, bar);
                 if (++s == stages) { s = 0; ph ^= 1u; }
             }
-            if (j < my)      // gave up: let the copies already issued land
-                for (int64_t k = (j > stages ? j - stages : 0); k < j; k++)
-                    for (uint32_t it = 0; it < ZERO_TMA_WAIT_LIMIT &&
-                                          !mbar_try_wait(smem_u32(&sh.full[k % stages]),
-                                                         (uint32_t)((k / stages) & 1));
-                         it++) {
-                    }
+            issued = j;
         }
     } else {                                                // consumers: elements 4t..4t+3
         const int t = threadIdx.x;
@@ -232,6 +228,20 @@ __global__ void __launch_bounds__(ZERO_TMA_THREADS, 1) k_reduce_tma(const StepAr
             }
         }
     }
+    // Every consumer has left its loop, so the abort flag is final.  After an
+    // abort, whichever side gave up and however the producer's loop ended, only
+    // the last `stages` issued tiles can still have copies in flight (an earlier
+    // tile's stage was reissued only after its consumers released it, which
+    // needs its copies complete): wait, bounded, for those to land before the
+    // block reuses or releases its shared memory.
+    __syncthreads();
+    if (warp == 8 && lane == 0 && *(volatile int*)&sh.abort_flag)
+        for (int64_t k = (issued > stages ? issued - stages : 0); k < issued; k++)
+            for (uint32_t it = 0; it < ZERO_TMA_WAIT_LIMIT &&
+                                  !mbar_try_wait(smem_u32(&sh.full[k % stages]),
+                                                 (uint32_t)((k / stages) & 1));
+                 it++) {
+            }
     const double bsum = block_sum_w(acc, sh.d);
     const int bbad = block_or_w(bad, sh.i);
     if (threadIdx.x == 0) {
