@@ -16,7 +16,8 @@
  *       ([L18] 2.2, 2.5; [PZ] 5.2);
  *   (2) unscale by the loss scale; any inf/NaN sets the overflow flag, which
  *       under dynamic loss scaling skips the step and halves the scale
- *       ([L32] 4.3);
+ *       ([L32] 4.3), and under a static scale skips it when the caller asks
+ *       (zero_hparams_t.skip_on_overflow);
  *   (3) global gradient norm over every shard and clip-by-norm
  *       ([L32] 4.2 "gradient_clipping");
  *   (4) Adam / AdamW with bias correction on each shard's fp32 master, m, v
@@ -84,8 +85,28 @@ typedef enum { ZERO_FP16 = 0, ZERO_BF16 = 1 } zero_dtype_t;
  *                            t unchanged) and multiplies S by backoff; after
  *                            growth_interval good steps in a row S doubles
  *                            (growth_interval <= 0: never).  Requires fp16.
- *                            0: static S; the overflow flag is reported but
- *                            does not skip. */
+ *                            0: static S (see skip_on_overflow).
+ *   skip_on_overflow         with a static S: 1 = an overflow skips the step
+ *                            (state untouched, t and S unchanged); 0 = the
+ *                            flag is reported and the step goes ahead.
+ *                            Ignored under dynamic_scale (which always skips).
+ *
+ * Overflow under a static scale (dynamic_scale 0, skip_on_overflow 0): the
+ * skip belongs to loss scaling ([L32] 4.3 ties a NaN loss to the fp16
+ * loss_scale setting), and a step that nothing global gates is what lets the
+ * update run as one fused pass over the data.  The consequences of a non-finite
+ * averaged gradient element i in such a step:
+ *   - without clipping, only element i is affected: its master, m and v
+ *     become NaN (or inf) and stay so; every other element is updated exactly
+ *     as if element i's gradient had been finite;
+ *   - with clipping, the norm is inf, the clip coefficient tau/inf = 0, so
+ *     every finite element takes a zero-gradient step (m *= beta1,
+ *     v *= beta2, the master moves by the remaining momentum) and element i
+ *     becomes NaN (inf * 0).
+ * A caller who wants such steps dropped sets skip_on_overflow = 1; the plan
+ * then runs two passes (the flag must be known before any update), which
+ * costs the fp32 gradient's write and read (8 bytes per element) on the
+ * paths that would otherwise fuse. */
 typedef struct {
     float lr, beta1, beta2, eps, weight_decay;
     int   decoupled_wd;
@@ -94,6 +115,7 @@ typedef struct {
     int   dynamic_scale;
     float backoff;
     int   growth_interval;
+    int   skip_on_overflow;
 } zero_hparams_t;
 
 /* ---- plans ------------------------------------------------------------ */
@@ -450,8 +472,9 @@ zero_status_t zero_plan_kernel_times(zero_plan_t plan, double* reduce_ms, double
                                      int64_t* steps, int64_t* launches);
 
 /* Which kernel path the plan runs: 0 = fused single pass (no clip, no dynamic
- * scale), 1 = two passes through an fp32 gradient in the workspace, 2 = two
- * passes that re-read the 16-bit gradients (clip or dynamic scale, nd < 4). */
+ * scale, no skip_on_overflow), 1 = two passes through an fp32 gradient in the
+ * workspace, 2 = two passes that re-read the 16-bit gradients (clip, dynamic
+ * scale or skip_on_overflow, nd < 4). */
 int zero_plan_path(zero_plan_t plan);
 
 /* Which kernel runs the reduce pass of a two-pass plan: 0 = 128-bit loads of

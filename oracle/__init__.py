@@ -47,7 +47,7 @@ class Hparams(ctypes.Structure):
                 ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float),
                 ("decoupled_wd", ctypes.c_int), ("clip_norm", ctypes.c_float),
                 ("dynamic_scale", ctypes.c_int), ("backoff", ctypes.c_float),
-                ("growth_interval", ctypes.c_int)]
+                ("growth_interval", ctypes.c_int), ("skip_on_overflow", ctypes.c_int)]
 
 
 class Scalars(ctypes.Structure):
@@ -78,11 +78,12 @@ class Opt:
     dynamic_scale: int = 0
     backoff: float = 0.5
     growth_interval: int = 1000
+    skip_on_overflow: int = 0
 
     def c(self) -> Hparams:
         return Hparams(self.lr, self.beta1, self.beta2, self.eps, self.weight_decay,
                        self.decoupled_wd, self.clip_norm, self.dynamic_scale,
-                       self.backoff, self.growth_interval)
+                       self.backoff, self.growth_interval, self.skip_on_overflow)
 
 
 def new_scalars(loss_scale: float = 1.0) -> Scalars:

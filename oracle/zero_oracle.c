@@ -217,11 +217,14 @@ float zo_clip_coef(double norm, float clip)
 void zo_advance(const zo_hparams* hp, zo_scalars* st, int overflow, zo_result* res)
 {
     res->overflow = overflow;
-    if (overflow && hp->dynamic_scale) {
-        /* skipped step: nothing moves except the loss scale */
+    if (overflow && (hp->dynamic_scale || hp->skip_on_overflow)) {
+        /* skipped step: nothing moves except, under dynamic scaling, the
+         * loss scale, which backs off */
         res->skipped  = 1;
-        st->loss_scale = st->loss_scale * hp->backoff;
-        st->good_steps = 0;
+        if (hp->dynamic_scale) {
+            st->loss_scale = st->loss_scale * hp->backoff;
+            st->good_steps = 0;
+        }
         res->bc1 = res->bc2 = 0.0f;
         return;
     }

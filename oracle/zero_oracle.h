@@ -73,6 +73,10 @@ typedef struct {
                                loss scale off; growth after good steps     */
     float backoff;          /* scale multiplier on overflow                 */
     int   growth_interval;  /* good steps before the scale doubles; <=0 off */
+    int   skip_on_overflow; /* 1: an overflow skips the step under a static
+                               scale too (the scale is left as it is); 0:
+                               under a static scale the flag is only
+                               reported and the step goes ahead            */
 } zo_hparams;
 
 typedef struct {            /* optimizer scalars carried across steps       */

@@ -45,12 +45,16 @@ def at(t, idx_t):
     return t.index_select(0, idx_t).cpu().numpy()
 
 
-def test_gpt2_1p5b_nd16_full_size(z):
+def test_gpt2_1p5b_nd16_full_schedule(z):
     """GPT-2 1.5B, Nd = 16, ZeRO-2, fp16 x65536 dynamic, clip 1.0 -- the bench
-    workload.  Step 1 normal, step 2 with +inf planted (skipped, scale halved),
-    step 3 normal at the new scale."""
+    workload at its own schedule: 10 steps, +inf planted at steps 3 and 7, so
+    those two are skipped and the scale goes 65536 -> 32768 -> 16384 (each step's
+    gradients generated at the scale in force).  Every non-skipped step's global
+    norm is the oracle's, streamed over all 25 G gradient values; the sampled
+    elements (65 K plus every shard boundary) follow all 10 steps."""
     import torch
     w = W.gpt2_xl()
+    assert (w.steps, tuple(w.inf_steps)) == (10, (3, 7))
     dev = torch.device("cuda", 0)
     sp = torch.cuda.current_stream().cuda_stream
     plan = z.zero_plan_create(w.psi, w.nd, w.stage, w.dtype, w.shapes, hp_of(z, w))
@@ -70,7 +74,9 @@ def test_gpt2_1p5b_nd16_full_size(z):
         mm, vs = np.zeros_like(ms), np.zeros_like(ms)
         ps = np.zeros(idx.size, np.uint16)
         st, opt, scale = oracle.new_scalars(w.loss_scale), opt_of(w), w.loss_scale
-        for step, inject in ((1, False), (2, True), (3, False)):
+        skips = []
+        for step in range(1, w.steps + 1):
+            inject = step in w.inf_steps
             site = gen.inf_site(w.seed, step, w.psi, w.nd) if inject else None
             gen.cuda_ranks_16(grads.data_ptr(), w.seed, gen.STREAM_GRAD, step, w.nd, w.psi,
                               w.grad_sigma, scale, w.dtype, rank_stride=padded, cuda_stream=sp)
@@ -83,17 +89,21 @@ def test_gpt2_1p5b_nd16_full_size(z):
                 g16 = H.oracle_sampled_grads(w.seed, step, w.nd, np.array([site[1]]), w.grad_sigma,
                                              scale, w.dtype, inf_at=site)
                 _, ovf = oracle.reduce(w.nd, w.dtype, g16, loss_scale=scale)
+                assert ovf
                 norm = float("inf")
             else:
                 norm, ovf = H.oracle_norm_streamed(w.seed, step, w.nd, w.psi, w.grad_sigma,
                                                    scale, w.dtype)
+                assert not ovf
             c = oracle.clip_coef(norm, w.clip)
             res = oracle.advance(opt, st, ovf)
-            assert r["skipped"] == res.skipped == int(inject)
-            assert (r["t"], r["loss_scale"]) == (st.t, st.loss_scale)
+            skips.append(r["skipped"])
+            assert r["skipped"] == res.skipped == int(inject), f"step {step}"
+            assert z.zero_step_overflow(plan) == int(ovf)
+            assert (r["t"], r["loss_scale"]) == (st.t, st.loss_scale), f"step {step}"
             if not res.skipped:
-                assert abs(r["grad_norm"] - norm) <= H.REL_NORM * norm
-                assert abs(r["clip_coef"] - c) <= 4e-7 * c
+                assert abs(r["grad_norm"] - norm) <= H.REL_NORM * norm, f"step {step}"
+                assert abs(r["clip_coef"] - c) <= 4e-7 * c, f"step {step}"
                 g16 = H.oracle_sampled_grads(w.seed, step, w.nd, idx, w.grad_sigma, scale, w.dtype)
                 g, _ = oracle.reduce(w.nd, w.dtype, g16, loss_scale=scale)
                 # the reduced gradient in the workspace is bit-exact at every sample
@@ -105,6 +115,8 @@ def test_gpt2_1p5b_nd16_full_size(z):
                                   at(params, idx_t).view(np.uint16)), (ms, mm, vs, ps),
                                  f"gpt2-1.5b step {step}")
             scale = st.loss_scale
+        assert skips == [0, 0, 1, 0, 0, 0, 1, 0, 0, 0]
+        assert (st.t, st.loss_scale) == (8, 16384.0)
     finally:
         z.zero_plan_destroy(plan)
 
@@ -154,10 +166,11 @@ def test_gpt2_small_nd8_full_size_all_elements(z):
 
 def test_llama3_8b_nd64_stage3_full_size(z):
     """LLaMA-3-8B, Nd = 64, ZeRO-3: rank 0's shard (125.5 M elements) updated
-    from its 64 contributions (sampled against the oracle), then one full
-    transformer-layer unit gathered from the 64 shards (every element against
-    the oracle's concatenation) and the embedding and head units (ranks 1-63's
-    parts in full, rank 0's part against rank 0's shard)."""
+    from its 64 contributions (sampled against the oracle), then every one of
+    the 34 units (embedding, 32 transformer layers, final norm + head) gathered
+    from the 64 shards and compared in full with the oracle's concatenation:
+    rank 0's slice of each unit from the oracle's step on that slice, ranks
+    1-63's slices from the seeded shard generator."""
     import torch
     w = W.llama3_8b()
     dev = torch.device("cuda", 0)
@@ -195,35 +208,26 @@ def test_llama3_8b_nd64_stage3_full_size(z):
             gen.cuda_s16(s.data_ptr(), w.seed, gen.STREAM_SHARD, 0, k, total, w.master_sigma, 1.0,
                          w.dtype, cuda_stream=sp)
             shards.append(s)
-        # one transformer layer, every element against the oracle
-        ln, sl, off = z.zero_plan_unit(plan, 1)
-        out = torch.empty(ln, dtype=torch.int16, device=dev)
-        z.zero_gather_layer(plan, 1, shards, out, sp)
-        torch.cuda.synchronize()
-        g16 = gen.ranks_16_mt(w.seed, gen.STREAM_GRAD, 1, w.nd, sl, w.grad_sigma, 1.0, w.dtype,
-                              index0=off)
-        om = gen.f32(w.seed, gen.STREAM_MASTER, 0, 0, sl, w.master_sigma, index0=off)
-        r0 = np.zeros(sl, np.uint16)
-        oracle.step_sharded(w.nd, w.dtype, g16, om, np.zeros_like(om), np.zeros_like(om), r0,
-                            opt_of(w), oracle.new_scalars(), nthreads=16)
-        del g16
-        slices = [r0] + [gen.s16(w.seed, gen.STREAM_SHARD, 0, k, sl, w.master_sigma, 1.0, w.dtype,
-                                 index0=off) for k in range(1, w.nd)]
-        want = oracle.gather_unit(w.nd, ln, sl, slices)
-        got = out.cpu().numpy().view(np.uint16)
-        assert np.array_equal(got, want)            # no clip: the update is bit-exact
-        # embedding and head units
-        for u in (0, nunits - 1):
+        # every unit, every element, against the oracle
+        for u in range(nunits):
             ln, sl, off = z.zero_plan_unit(plan, u)
             out = torch.empty(ln, dtype=torch.int16, device=dev)
             z.zero_gather_layer(plan, u, shards, out, sp)
-            torch.cuda.synchronize()
+            g16 = gen.ranks_16_mt(w.seed, gen.STREAM_GRAD, 1, w.nd, sl, w.grad_sigma, 1.0,
+                                  w.dtype, index0=off)
+            om = gen.f32(w.seed, gen.STREAM_MASTER, 0, 0, sl, w.master_sigma, index0=off)
+            r0 = np.zeros(sl, np.uint16)
+            oracle.step_sharded(w.nd, w.dtype, g16, om, np.zeros_like(om), np.zeros_like(om), r0,
+                                opt_of(w), oracle.new_scalars(), nthreads=16)
+            del g16, om
+            slices = gen.ranks_16_mt(w.seed, gen.STREAM_SHARD, 0, w.nd, sl, w.master_sigma, 1.0,
+                                     w.dtype, index0=off)
+            slices[0] = r0
+            want = oracle.gather_unit(w.nd, ln, sl, list(slices))
+            del slices
             got = out.cpu().numpy().view(np.uint16)
-            assert np.array_equal(got[:sl], params[off:off + sl].cpu().numpy().view(np.uint16))
-            for k in (1, 2, 31, 63):
-                want = gen.s16(w.seed, gen.STREAM_SHARD, 0, k, sl, w.master_sigma, 1.0, w.dtype,
-                               index0=off)
-                assert np.array_equal(got[k * sl:(k + 1) * sl], want)
+            assert np.array_equal(got, want), f"unit {u}"   # no clip: the update is bit-exact
+            del out, got, want
     finally:
         z.zero_plan_destroy(plan)
 

@@ -155,13 +155,48 @@ def test_nan_and_inf_skip_and_scale_schedule(z):
     assert [r["loss_scale"] for r in gpu.results] == [1024, 512, 512, 1024, 512, 512, 1024]
 
 
-def test_static_scale_reports_overflow(z):
-    c = H.Case(shapes=[(5000,)], nd=4, dtype=gen.FP16, grad_sigma=1e-3, loss_scale=8.0,
-               steps=2, inf_steps=(2,), clip=1.0)
-    gpu = H.run_gpu(z, c)
-    assert [r["overflow"] for r in gpu.results] == [0, 1]
-    assert [r["skipped"] for r in gpu.results] == [0, 0]
-    assert gpu.results[-1]["t"] == 2
+STATIC_OVERFLOW = {
+    # name: (case settings, kernel path the plan must take)
+    "fused-no-clip": (dict(nd=8, dtype=gen.BF16), 0),
+    "two-pass-clip": (dict(nd=8, dtype=gen.BF16, clip=1.0), 1),
+    "recompute-clip": (dict(nd=2, dtype=gen.BF16, clip=1.0), 2),
+    "fp16-scaled-clip": (dict(nd=4, dtype=gen.FP16, grad_sigma=1e-3, loss_scale=8.0, clip=1.0),
+                         1),
+    "skip-on-overflow": (dict(nd=4, dtype=gen.FP16, grad_sigma=1e-3, loss_scale=8.0,
+                              skip_on_overflow=1), 1),
+    "skip-on-overflow-recompute": (dict(nd=3, dtype=gen.BF16, skip_on_overflow=1, clip=1.0), 2),
+}
+
+
+@pytest.mark.parametrize("name", sorted(STATIC_OVERFLOW))
+def test_static_scale_overflow_against_the_oracle(z, name):
+    """Overflow under a static loss scale, against the oracle's state and
+    results over the steps that follow: without skip_on_overflow the flag is
+    reported and the step goes ahead (no clip: only the planted element turns
+    non-finite; clip: tau / inf = 0 makes every other element take a
+    zero-gradient step); with it the step is skipped and the scale kept.  +inf
+    at step 2, NaN at step 4, 5 steps; without a clip every other element is
+    bit-exact, with one within the state tolerances."""
+    over, path = STATIC_OVERFLOW[name]
+    c = H.Case(shapes=[(40_000,), (1_003,)], steps=5, inf_steps=(2,), nan_steps=(4,), **over)
+    plan = z.zero_plan_create(c.psi, c.nd, c.stage, c.dtype, c.shapes, c.hparams(z))
+    assert z.zero_plan_path(plan) == path
+    z.zero_plan_destroy(plan)
+    gpu, ora = check(z, c)
+    assert [r["overflow"] for r in gpu.results] == [0, 1, 0, 1, 0]
+    skip = c.skip_on_overflow
+    assert [r["skipped"] for r in gpu.results] == [0, skip, 0, skip, 0]
+    assert gpu.results[-1]["t"] == (3 if skip else 5)
+    assert all(r["loss_scale"] == c.loss_scale for r in gpu.results)
+    bad = np.isnan(ora.master)
+    assert bad.any() == (not skip) and np.array_equal(bad, np.isnan(gpu.master))
+    if not skip and not c.clip:
+        assert bad.sum() == 2                      # the two planted elements only
+    if not c.clip:           # with a clip, c may differ in its last bit (the norm's rounding)
+        for a, b in zip((gpu.master, gpu.m, gpu.v), (ora.master, ora.m, ora.v)):
+            keep = ~(np.isnan(a) & np.isnan(b))
+            assert np.array_equal(a[keep].view(np.uint32), b[keep].view(np.uint32))
+        assert np.array_equal(gpu.params[~bad], ora.params[~bad])
 
 
 def test_empty_model(z):

@@ -37,6 +37,10 @@ MUTANTS = {
     "skip-keeps-scale": ("st->loss_scale = st->loss_scale * hp->backoff;",
                          "st->loss_scale = st->loss_scale;"),
     "skip-advances-t": ("res->skipped  = 1;", "res->skipped  = 1; st->t = st->t + 1;"),
+    "static-skip-ignored": ("if (overflow && (hp->dynamic_scale || hp->skip_on_overflow)) {",
+                            "if (overflow && hp->dynamic_scale) {"),
+    "static-skip-backs-off": ("        if (hp->dynamic_scale) {\n            st->loss_scale",
+                              "        {\n            st->loss_scale"),
     "round-ties-away": ("if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;\n    return r * q;",
                         "if (frac > 0.5 || (frac == 0.5)) r += 1.0;\n    return r * q;"),
     "qwz-round-ties-away": ("if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;\n    return (int32_t)r;",

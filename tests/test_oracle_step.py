@@ -277,6 +277,101 @@ def test_static_scale_reports_overflow_without_skipping(oracle):
     assert r["overflow"] == 1 and r["skipped"] == 0 and st.t == 1 and st.loss_scale == 8.0
 
 
+def _warm_state(oracle, nd, n, dtype, opt, seed):
+    """state after one ordinary step, so m and v are nonzero"""
+    rng = np.random.default_rng(seed)
+    master, m, v, params = state(n, seed)
+    st = oracle.new_scalars(1.0)
+    oracle.step(nd, dtype, bits16(dtype, rng.standard_normal((nd, n)) * 0.03), master, m, v,
+                params, opt, st)
+    return [master, m, v, params], st, rng
+
+
+@pytest.mark.parametrize("dtype", [FP16, BF16])
+def test_static_scale_overflow_without_clip_touches_only_its_element(oracle, dtype):
+    """With a static scale and no clip nothing global gates the update: the
+    non-finite element's state becomes non-finite, and every other element is
+    updated bit for bit as if that element's gradient had been finite."""
+    n, nd, site = 300, 4, (2, 77)
+    opt = oracle.Opt(dynamic_scale=0)
+    s0, st0, rng = _warm_state(oracle, nd, n, dtype, opt, 11)
+    grads = bits16(dtype, rng.standard_normal((nd, n)) * 0.03)
+    bad = grads.copy()
+    bad[site] = bits16(dtype, [np.inf])[0]
+    fine = grads.copy()
+    fine[site] = 0
+    a = [x.copy() for x in s0]
+    b = [x.copy() for x in s0]
+    sa, sb = oracle.new_scalars(1.0), oracle.new_scalars(1.0)
+    for sx in (sa, sb):
+        sx.t, sx.beta1_pow, sx.beta2_pow = st0.t, st0.beta1_pow, st0.beta2_pow
+    ra = oracle.step(nd, dtype, bad, *a, opt, sa)
+    rb = oracle.step(nd, dtype, fine, *b, opt, sb)
+    assert ra["overflow"] == 1 and ra["skipped"] == 0 and rb["overflow"] == 0
+    assert sa.t == sb.t == 2
+    assert not np.isfinite(ra["grad_norm"]) and ra["clip_coef"] == 1.0
+    keep = np.arange(n) != site[1]
+    for x, y in zip(a, b):
+        assert np.array_equal(x[keep], y[keep])
+    # g = +inf: m and v become +inf, the update inf/inf = NaN reaches the master
+    assert np.isposinf(a[1][site[1]]) and np.isposinf(a[2][site[1]]) and np.isnan(a[0][site[1]])
+
+
+def test_static_scale_overflow_with_clip_is_a_zero_gradient_step(oracle):
+    """With a static scale and clipping, a non-finite gradient makes the norm
+    infinite and the clip coefficient tau / inf = 0: every finite element takes
+    exactly the step a zero gradient gives (m *= beta1, v *= beta2, the master
+    moves by the remaining momentum), and the non-finite element becomes NaN
+    (inf * 0)."""
+    n, nd, site = 256, 3, (0, 200)
+    opt = oracle.Opt(dynamic_scale=0, clip_norm=1.0)
+    s0, st0, rng = _warm_state(oracle, nd, n, BF16, opt, 12)
+    assert np.count_nonzero(s0[1]) == n
+    bad = bf16(rng.standard_normal((nd, n)) * 0.03)
+    bad[site] = bf16([np.inf])[0]
+    zero = np.zeros((nd, n), np.uint16)
+    a = [x.copy() for x in s0]
+    b = [x.copy() for x in s0]
+    sa, sb = oracle.new_scalars(1.0), oracle.new_scalars(1.0)
+    for sx in (sa, sb):
+        sx.t, sx.beta1_pow, sx.beta2_pow = st0.t, st0.beta1_pow, st0.beta2_pow
+    ra = oracle.step(nd, BF16, bad, *a, opt, sa)
+    rb = oracle.step(nd, BF16, zero, *b, opt, sb)
+    assert ra["overflow"] == 1 and ra["skipped"] == 0 and ra["clip_coef"] == 0.0
+    assert rb["grad_norm"] == 0.0 and rb["clip_coef"] == 1.0
+    keep = np.arange(n) != site[1]
+    for x, y in zip(a, b):
+        assert np.array_equal(x[keep], y[keep])
+    b1 = np.float32(0.9)
+    assert np.array_equal(a[1][keep], (b1 * s0[1][keep]).astype(np.float32))   # m *= beta1
+    assert np.isnan(a[0][site[1]]) and np.isnan(a[1][site[1]]) and np.isnan(a[2][site[1]])
+
+
+@pytest.mark.parametrize("clip", [0.0, 1.0])
+def test_skip_on_overflow_under_a_static_scale(oracle, clip):
+    """skip_on_overflow = 1 with a static scale: an overflow skips the step
+    (state bit-unchanged, t unchanged) and the scale is not backed off; the
+    next clean step proceeds as step t + 1."""
+    n, nd = 200, 4
+    opt = oracle.Opt(dynamic_scale=0, skip_on_overflow=1, clip_norm=clip)
+    s0, st, rng = _warm_state(oracle, nd, n, FP16, opt, 13)
+    st.loss_scale = 4.0
+    snap = [x.copy() for x in s0]
+    bad = f16(rng.standard_normal((nd, n)) * 0.03 * 4.0)
+    bad[1, 3] = f16([np.nan])[0]
+    r = oracle.step(nd, FP16, bad, *s0, opt, st)
+    assert r["overflow"] == 1 and r["skipped"] == 1
+    assert (st.t, st.loss_scale, st.good_steps) == (1, 4.0, 0)
+    for x, y in zip(snap, s0):
+        assert np.array_equal(x, y)
+    good = f16(rng.standard_normal((nd, n)) * 0.03 * 4.0)
+    r = oracle.step(nd, FP16, good, *s0, opt, st)
+    assert r["skipped"] == 0 and st.t == 2 and st.loss_scale == 4.0
+    # without skip_on_overflow the same overflow is reported and not skipped
+    r = oracle.step(nd, FP16, bad, *s0, oracle.Opt(dynamic_scale=0, clip_norm=clip), st)
+    assert r["overflow"] == 1 and r["skipped"] == 0 and st.t == 3 and st.loss_scale == 4.0
+
+
 # ------------------------------------------ sharded == unsharded (L18 2.5)
 def _seq(rng, nd, n, steps, dtype):
     return [bits16(dtype, rng.standard_normal((nd, n)) * 10.0 ** rng.uniform(-4, 0))

@@ -51,14 +51,16 @@ class zero_hparams_t(ctypes.Structure):
                 ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float),
                 ("decoupled_wd", ctypes.c_int), ("clip_norm", ctypes.c_float),
                 ("loss_scale", ctypes.c_float), ("dynamic_scale", ctypes.c_int),
-                ("backoff", ctypes.c_float), ("growth_interval", ctypes.c_int)]
+                ("backoff", ctypes.c_float), ("growth_interval", ctypes.c_int),
+                ("skip_on_overflow", ctypes.c_int)]
 
 
 def hparams(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0, decoupled_wd=1,
             clip_norm=0.0, loss_scale=1.0, dynamic_scale=0, backoff=0.5,
-            growth_interval=1000) -> zero_hparams_t:
+            growth_interval=1000, skip_on_overflow=0) -> zero_hparams_t:
     return zero_hparams_t(lr, beta1, beta2, eps, weight_decay, decoupled_wd, clip_norm,
-                          loss_scale, dynamic_scale, backoff, growth_interval)
+                          loss_scale, dynamic_scale, backoff, growth_interval,
+                          skip_on_overflow)
 
 
 _lock = threading.Lock()

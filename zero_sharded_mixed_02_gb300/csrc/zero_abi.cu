@@ -252,7 +252,8 @@ zero_status_t create_impl(uint64_t psi, int nd, int stage, zero_dtype_t dtype,
     p->k.use_wd = hp->weight_decay != 0.0f;
 
     // kernel path
-    const bool needs_global = hp->clip_norm > 0.0f || hp->dynamic_scale;
+    // anything that must be known before the first update forces two passes
+    const bool needs_global = hp->clip_norm > 0.0f || hp->dynamic_scale || hp->skip_on_overflow;
     int kind_a, kind_b = -1;
     if (!needs_global) {
         p->path = PATH_FUSED;
@@ -364,6 +365,7 @@ StepArgs step_args(const zero_plan* plan, const void* grads, float* master, floa
     a.k = plan->k;
     a.clip = plan->hp.clip_norm;
     a.dynamic = plan->hp.dynamic_scale ? 1 : 0;
+    a.skip_static = plan->hp.skip_on_overflow ? 1 : 0;
     a.backoff = plan->hp.backoff;
     a.growth_interval = plan->hp.growth_interval;
     a.state = plan->d_state;

@@ -67,6 +67,7 @@ struct StepArgs {
     AdamK     k;
     float     clip;          // 0 = off
     int       dynamic;       // dynamic loss scaling: overflow skips + backoff
+    int       skip_static;   // static scale: an overflow skips the step too
     float     backoff;
     int       growth_interval;
     DevState* state;

@@ -49,10 +49,12 @@ static __device__ __noinline__ void finalize(const StepArgs a, double sumsq, int
                         ? __double2float_rn(__ddiv_rn((double)a.clip, st.grad_norm)) : 1.0f;
     st.err = S->st.err;        // sticky: a bounded wait that gave up, in any step
     st.pad = 0;
-    if (overflow && a.dynamic) {
+    if (overflow && (a.dynamic || a.skip_static)) {
         st.skipped = 1;
-        sc.loss_scale = __fmul_rn(sc.loss_scale, a.backoff);
-        sc.good_steps = 0;
+        if (a.dynamic) {                       // only a dynamic scale backs off
+            sc.loss_scale = __fmul_rn(sc.loss_scale, a.backoff);
+            sc.good_steps = 0;
+        }
         st.bc1 = st.bc2 = 0.0f;
     } else {
         st.skipped = 0;
@@ -244,7 +246,8 @@ __global__ void __launch_bounds__(ZERO_THREADS) k_update(const StepArgs a)
     }
 }
 
-// ---- fused single pass (no clip, no dynamic scale): stages 1-6a ------------
+// ---- fused single pass (no clip, no dynamic scale, no skip on overflow):
+// stages 1-6a ----------------------------------------------------------------
 template <int DT, int ND>
 __global__ void __launch_bounds__(ZERO_THREADS) k_fused(const StepArgs a)
 {
