@@ -779,11 +779,42 @@ def run_stage3(args):
             gather_all_q()
         t_q = _timed_steps(torch, stream, gather_all_q, K) / K
         q_bytes = (2 + bits / 8) * total + (bits / 8 + 2) * w.psi + 4 * w.psi / 256
+
+        # the qwZ step as one update pass that quantizes in its epilogue, then
+        # the quantized gathers
+        def update_q():
+            z.zero_step_qwz(plan, grads, master, m, v, params, None, bits, codes[0], scales[0],
+                            sp)
+
+        def gathers_q():
+            for u in range(nunits):
+                z.zero_gather_layer_q(plan, u, bits, cptr, sptr, out, sp)
+
+        def step_q():
+            update_q()
+            gathers_q()
+
+        for _ in range(2):
+            step_q()
+        t_uq = _timed_steps(torch, stream, update_q, K) / K
+        t_gq = _timed_steps(torch, stream, gathers_q, K) / K
+        t_sq = _timed_steps(torch, stream, step_q, K) / K
+        uq_bytes = (2 * w.nd + 26 + bits / 8 + 4 / 256) * total
+        gq_bytes = (bits / 8 + 2 + 4 / 256) * w.psi
         qwz = {"bits": bits, "block": 256, "quantize_and_gather_ms": t_q,
                "bytes_per_elem": bits / 8 + 2 + 4 / 256,
                "gbs": q_bytes / (t_q / 1e3) / 1e9,
                "vs_unquantized_gather": t_gat / t_q,
-               "frac_of_measured_hbm": q_bytes / (t_q / 1e3) / 1e9 / peak}
+               "frac_of_measured_hbm": q_bytes / (t_q / 1e3) / 1e9 / peak,
+               "fused_step": {
+                   "what": "zero_step_qwz (update + quantize in one pass) then the quantized "
+                           "gathers of every unit",
+                   "step_ms": t_sq, "update_q_ms": t_uq, "gathers_q_ms": t_gq,
+                   "update_q_gbs": uq_bytes / (t_uq / 1e3) / 1e9,
+                   "update_q_frac_of_measured_hbm": uq_bytes / (t_uq / 1e3) / 1e9 / peak,
+                   "gathers_q_frac_of_measured_hbm": gq_bytes / (t_gq / 1e3) / 1e9 / peak,
+                   "vs_unquantized_step": (t_upd + t_gat) / t_sq,
+                   "vs_separate_update_quantize_gather": (t_upd + t_q) / t_sq}}
     desc = DESCRIPTIONS.get(w.name, f"LLaMA-3-8B-shaped list scaled to {len(units) - 2} layers")
     print(json.dumps({
         "mode": "zero3", "metric": "ZeRO-3 step: resident-shard update and per-unit gathers",

@@ -280,6 +280,22 @@ zero_status_t zero_gather_layer_q(zero_plan_t plan, int unit, int bits,
                                   const void* const* code_ptrs, const float* const* scale_ptrs,
                                   void* out, void* stream);
 
+/* One ZeRO-3 optimizer step (exactly zero_step's, same arguments) whose update
+ * pass also quantizes the resident shard's updated 16-bit parameters for the
+ * qwZ gather ([L18] 4.5): codes and scales receive what
+ * zero_quantize_shard(dtype, params, L, bits, codes, scales) would write after
+ * the step, L being the shard length, but the parameters are quantized from
+ * the update's registers as they are written instead of being read back
+ * (2 bytes per element and one launch saved).  On a skipped step the
+ * unchanged parameters are quantized, so the codes are valid whatever the
+ * buffers held.  codes: L bytes (bits 8) or L/2 bytes (bits 4), 16-byte
+ * aligned; scales: ceil(L/256) floats.  Asynchronous.  Errors: ZERO_EINVAL
+ * (not stage 3, bits not 4 or 8, null or misaligned pointer), ZERO_ESTATE,
+ * ZERO_ECUDA. */
+zero_status_t zero_step_qwz(zero_plan_t plan, const void* grads, float* master, float* m, float* v,
+                            void* params, void* workspace, int bits, void* codes, float* scales,
+                            void* stream);
+
 /* ---- gradient norm without allocating ------------------------------------ */
 
 /* No counterpart on the pages: a convenience for callers that may not

@@ -17,7 +17,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libzero_b200.so")
 
-SOURCES = ["zero_abi.cu", "zero_step_fp16.cu", "zero_step_bf16.cu", "zero_gather.cu",
+SOURCES = ["zero_abi.cu", "zero_step_fp16.cu", "zero_step_bf16.cu", "zero_step_q_fp16.cu",
+           "zero_step_q_bf16.cu", "zero_gather.cu",
            "zero_noalloc.cu", "zero_qwz.cu", "zero_ckpt.cu", "zero_offload.cu",
            "zero_cpu_adam.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -55,6 +55,10 @@ struct zero_plan {
     int tma_stages = 0;
     uint64_t grid_b = 1;
     uint64_t workspace = 0;
+    // ZeRO-3 steps with the qwZ epilogue ([0]: 8 bits, [1]: 4 bits), resolved
+    // on first use: the single pass, or the update pass of the two-pass paths
+    const void* fn_q[2] = {nullptr, nullptr};
+    int grid_q[2] = {1, 1};
     // device
     int device = 0, sms = 1;
     DevState* d_state = nullptr;
@@ -491,6 +495,8 @@ void* const* plan_staging(zero_plan_t plan, int count, uint64_t bytes)
 
 const void* step_kernel(int dtype, int kind, int nd)
 {
+    if (kind >= K_FUSED_Q8)
+        return dtype == 0 ? step_kernel_q_fp16(kind, nd) : step_kernel_q_bf16(kind, nd);
     return dtype == 0 ? step_kernel_fp16(kind, nd) : step_kernel_bf16(kind, nd);
 }
 }  // namespace zero
@@ -710,11 +716,14 @@ zero_status_t zero_plan_set_reduce_kernel(zero_plan_t plan, int kind)
     return ZERO_OK;
 }
 
-zero_status_t zero_step(zero_plan_t plan, const void* grads, float* master, float* m, float* v,
-                        void* params, void* workspace, void* stream)
+}  // extern "C"
+
+namespace {
+
+// Validation shared by zero_step and zero_step_qwz.
+zero_status_t check_step_args(const zero_plan* plan, const void* grads, float* master, float* m,
+                              float* v, void* params, void* workspace)
 {
-    zero::TraceRange trace_("zero_step");
-    if (!plan) return ZERO_EINVAL;
     if (plan->poisoned) return ZERO_ESTATE;
     if (plan->n > 0) {
         const void* ptrs[] = {grads, master, m, v, params};
@@ -726,9 +735,16 @@ zero_status_t zero_step(zero_plan_t plan, const void* grads, float* master, floa
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return ZERO_ECUDA;
     if (dev != plan->device) return ZERO_EINVAL;
+    return ZERO_OK;
+}
 
-    StepArgs a = step_args(plan, grads, master, m, v, params, workspace);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
+// The step's launch sequence: pass 1 (fn_a; the fused pass, or the reduce pass
+// in the plan's configured form), then, on the two-pass paths, pass 2 (fn_b) as
+// its programmatic dependent; per-kernel events when profiling; the step's
+// completion event.
+zero_status_t launch_step(zero_plan* plan, StepArgs& a, const void* fn_a, int grid_a,
+                          const void* fn_b, cudaStream_t s)
+{
     ProfileSlot* slot = nullptr;
     if (plan->profile) {
         slot = &plan->ring[(size_t)(plan->ring_pos % PROFILE_RING)];
@@ -736,15 +752,16 @@ zero_status_t zero_step(zero_plan_t plan, const void* grads, float* master, floa
         plan->ring_pos++;
         if (cudaEventRecord(slot->ev[0], s) != cudaSuccess) return ZERO_ECUDA;
     }
+    const bool tma = plan->reduce_kernel && fn_a == plan->fn_a;
     int stages = plan->tma_stages;
     void* args_tma[] = {&a, &stages};
     void* args[] = {&a};
-    cudaError_t e = cudaLaunchKernel(plan->fn_a, dim3(plan->grid_a), dim3(plan->block_a),
-                                     plan->reduce_kernel ? args_tma : args, plan->smem_a, s);
+    cudaError_t e = cudaLaunchKernel(fn_a, dim3(grid_a), dim3(tma ? plan->block_a : ZERO_THREADS),
+                                     tma ? args_tma : args, tma ? plan->smem_a : 0, s);
     if (e != cudaSuccess) return ZERO_ECUDA;
     plan->launches++;
     if (slot && cudaEventRecord(slot->ev[1], s) != cudaSuccess) return ZERO_ECUDA;
-    if (plan->fn_b) {
+    if (fn_b) {
         // a programmatic dependent of pass 1: scheduled while pass 1 finishes, it
         // waits (griddepcontrol.wait) before reading what pass 1 wrote
         cudaLaunchAttribute attr[1];
@@ -757,18 +774,66 @@ zero_status_t zero_step(zero_plan_t plan, const void* grads, float* master, floa
         cfg.stream = s;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelExC(&cfg, plan->fn_b, args);
+        e = cudaLaunchKernelExC(&cfg, fn_b, args);
         if (e != cudaSuccess) return ZERO_ECUDA;
         plan->launches++;
     }
     if (slot) {
         if (cudaEventRecord(slot->ev[2], s) != cudaSuccess) return ZERO_ECUDA;
         slot->used = true;
-        slot->one_kernel = !plan->fn_b;
+        slot->one_kernel = !fn_b;
     }
     if (cudaEventRecord(plan->ev_done, s) != cudaSuccess) return ZERO_ECUDA;
     plan->stepped = true;
     return ZERO_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+zero_status_t zero_step(zero_plan_t plan, const void* grads, float* master, float* m, float* v,
+                        void* params, void* workspace, void* stream)
+{
+    zero::TraceRange trace_("zero_step");
+    if (!plan) return ZERO_EINVAL;
+    const zero_status_t st = check_step_args(plan, grads, master, m, v, params, workspace);
+    if (st != ZERO_OK) return st;
+    StepArgs a = step_args(plan, grads, master, m, v, params, workspace);
+    return launch_step(plan, a, plan->fn_a, plan->grid_a, plan->fn_b,
+                       static_cast<cudaStream_t>(stream));
+}
+
+zero_status_t zero_step_qwz(zero_plan_t plan, const void* grads, float* master, float* m,
+                            float* v, void* params, void* workspace, int bits, void* codes,
+                            float* scales, void* stream)
+{
+    zero::TraceRange trace_("zero_step_qwz");
+    if (!plan || plan->stage != 3 || (bits != 8 && bits != 4)) return ZERO_EINVAL;
+    const zero_status_t st = check_step_args(plan, grads, master, m, v, params, workspace);
+    if (st != ZERO_OK) return st;
+    if (plan->n > 0 && (!codes || !scales || !aligned16(codes) ||
+                        (reinterpret_cast<uintptr_t>(scales) & 3u) != 0))
+        return ZERO_EINVAL;
+    const int q = bits == 8 ? 0 : 1;
+    if (!plan->fn_q[q]) {
+        const int kind = plan->path == PATH_FUSED ? (q ? K_FUSED_Q4 : K_FUSED_Q8)
+                         : plan->path == PATH_G32 ? (q ? K_UPDATE_G32_Q4 : K_UPDATE_G32_Q8)
+                                                  : (q ? K_UPDATE_RECOMPUTE_Q4
+                                                       : K_UPDATE_RECOMPUTE_Q8);
+        const void* fn = step_kernel((int)plan->dtype, kind, plan->nd);
+        if (!fn) return ZERO_EINVAL;
+        plan->grid_q[q] = plan->path == PATH_FUSED
+                              ? grid_reduce(fn, plan->sms, plan->n, FUSED_WAVES) : 0;
+        plan->fn_q[q] = fn;
+    }
+    StepArgs a = step_args(plan, grads, master, m, v, params, workspace);
+    a.qcodes = static_cast<uint8_t*>(codes);
+    a.qscales = scales;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (plan->path == PATH_FUSED) return launch_step(plan, a, plan->fn_q[q], plan->grid_q[q],
+                                                     nullptr, s);
+    return launch_step(plan, a, plan->fn_a, plan->grid_a, plan->fn_q[q], s);
 }
 
 zero_status_t zero_step_result(zero_plan_t plan, int* skipped, double* grad_norm,

@@ -71,6 +71,10 @@ struct StepArgs {
     float     backoff;
     int       growth_interval;
     DevState* state;
+    // ZeRO-3 step with the qwZ quantizer in its epilogue: the updated 16-bit
+    // parameters' block codes and scales (as zero_quantize_shard writes them)
+    uint8_t*  qcodes = nullptr;
+    float*    qscales = nullptr;
     // bucketed step: the reduce pass covers one bucket and records its partial
     int       bucket = -1;                // -1: a whole step
     double*   bucket_partial = nullptr;   // [nbuckets] squared-norm partial of each bucket

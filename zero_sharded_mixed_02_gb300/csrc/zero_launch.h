@@ -14,7 +14,14 @@ enum Kind {
     K_UPDATE_RECOMPUTE = 3,  // pass 2 re-reading the 16-bit gradients (nd < 4)
     K_FUSED = 4,             // single pass (no clip, no dynamic scale)
     K_REDUCE_G32_TMA = 5,    // pass 1 with TMA bulk staging of the rank rows (runtime nd)
-    K_BUCKET_FINALIZE = 6    // bucketed step: norm and bookkeeping from the bucket partials
+    K_BUCKET_FINALIZE = 6,   // bucketed step: norm and bookkeeping from the bucket partials
+    // ZeRO-3 steps with the qwZ quantizer in the update's epilogue (8 or 4 bits)
+    K_FUSED_Q8 = 7,
+    K_FUSED_Q4 = 8,
+    K_UPDATE_G32_Q8 = 9,
+    K_UPDATE_G32_Q4 = 10,
+    K_UPDATE_RECOMPUTE_Q8 = 11,
+    K_UPDATE_RECOMPUTE_Q4 = 12
 };
 
 // Kernel function for (dtype, kind, nd); nullptr if that combination is not
@@ -23,6 +30,8 @@ const void* step_kernel(int dtype, int kind, int nd);
 
 const void* step_kernel_fp16(int kind, int nd);
 const void* step_kernel_bf16(int kind, int nd);
+const void* step_kernel_q_fp16(int kind, int nd);   // the K_*_Q* kinds
+const void* step_kernel_q_bf16(int kind, int nd);
 
 struct GatherArgs {
     const uint16_t* src[ZERO_MAX_ND];   // rank k's slice of the unit

@@ -10,6 +10,7 @@
 #pragma once
 
 #include "zero_common.cuh"
+#include "zero_qwz.cuh"
 
 namespace zero {
 
@@ -184,6 +185,48 @@ __global__ void __launch_bounds__(ZERO_THREADS, 4) k_reduce(const StepArgs a)
     reduce_and_finalize(a, acc, bad, sh);
 }
 
+// ---- qwZ epilogue: the updated 16-bit parameters quantized block by block ----
+// x: a lane's 16-bit parameters widened back to binary32 (0 for elements past
+// the shard's end).  The ZERO_QBLOCK-element block's absmax is a warp shuffle
+// reduction, then (when a block spans W warps) a shared-memory combine; the
+// codes and the scale are those codes_n / zero_quantize_shard give.
+template <int QB, int N, int W>
+static __device__ __forceinline__ void quant_epilogue(const float (&x)[N], int64_t e0, bool live,
+                                                      const StepArgs& a, float* sh_amax)
+{
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < N; i++) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    if constexpr (W > 1) {
+        const int w = threadIdx.x >> 5;
+        if ((threadIdx.x & 31) == 0) sh_amax[w] = amax;
+        __syncthreads();
+        const int w0 = w - w % W;
+#pragma unroll
+        for (int k = 0; k < W; k++) amax = fmaxf(amax, sh_amax[w0 + k]);
+    }
+    const float scale = __fdiv_rn(amax, QMax<QB>::v);
+    if (live && (e0 % ZERO_QBLOCK) == 0) a.qscales[e0 / ZERO_QBLOCK] = scale;
+    uint32_t c[N];
+    codes_n<QB, N>(x, scale, c);
+    if (!live) return;
+    if constexpr (N == 8) {
+        store8<QB>(a.qcodes, INT64_MAX, e0, c);
+    } else {                                           // N == 4
+        if (QB == 8) {
+            *reinterpret_cast<uint32_t*>(a.qcodes + e0) =
+                __byte_perm(__byte_perm(c[0], c[1], 0x0040), __byte_perm(c[2], c[3], 0x0040),
+                            0x5410);
+        } else {
+            *reinterpret_cast<uint16_t*>(a.qcodes + e0 / 2) =
+                (uint16_t)((c[0] & 0xFu) | ((c[1] & 0xFu) << 4) | ((c[2] & 0xFu) << 8) |
+                           ((c[3] & 0xFu) << 12));
+        }
+    }
+}
+
 // ---- pass 2: stages 4-6a (clip, Adam, cast, write-back) -------------------
 // One thread per 4 consecutive elements, one launch-wide block per 1024
 // elements (not a persistent grid: measured faster for this read-write mix).
@@ -192,7 +235,11 @@ __global__ void __launch_bounds__(ZERO_THREADS, 4) k_reduce(const StepArgs a)
 // recomputing, the 16-bit gradients' rank-order sums) are loaded first, since
 // pass 1 does not write them; griddepcontrol.wait then waits for pass 1 to
 // complete before the step status and the fp32 gradient are read.
-template <int DT, int ND, bool RECOMPUTE>
+// QB = 8 or 4: the qwZ epilogue (ZeRO-3 shards only, whose length is a multiple
+// of 64, so there is no ragged tail); a 256-element block is two warps.  On a
+// skipped step the unchanged parameters are quantized, so the codes are valid
+// whatever the buffers held.
+template <int DT, int ND, bool RECOMPUTE, int QB = 0>
 __global__ void __launch_bounds__(ZERO_THREADS) k_update(const StepArgs a)
 {
     const int nd = ND > 0 ? ND : a.nd;
@@ -211,6 +258,44 @@ __global__ void __launch_bounds__(ZERO_THREADS) k_update(const StepArgs a)
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const DevStatus st = a.state->st;
+    if constexpr (QB != 0) {
+        __shared__ float sh_amax[ZERO_THREADS / 32];
+        if (st.err) return;
+        float x[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        const bool live = vi < nvec;
+        if (st.skipped) {                              // quantize the unchanged parameters
+            if (live) {
+                const uint2 w = __ldcs(reinterpret_cast<const uint2*>(a.params) + vi);
+                widen2<DT>(w.x, x[0], x[1]);
+                widen2<DT>(w.y, x[2], x[3]);
+            }
+        } else if (live) {
+            const float c = st.clip_coef, bc1 = st.bc1, bc2 = st.bc2;
+            float g[4];
+            if (RECOMPUTE) {
+                Unscale un;
+                un.init(nd, st.used_scale);
+#pragma unroll
+                for (int e = 0; e < 4; e++) g[e] = un(s[e]);
+            } else {
+                const float4 g4 = __ldcs(reinterpret_cast<const float4*>(a.g32) + vi);
+                g[0] = g4.x; g[1] = g4.y; g[2] = g4.z; g[3] = g4.w;
+            }
+            adam1(g[0], c, p.x, m.x, v.x, bc1, bc2, a.k);
+            adam1(g[1], c, p.y, m.y, v.y, bc1, bc2, a.k);
+            adam1(g[2], c, p.z, m.z, v.z, bc1, bc2, a.k);
+            adam1(g[3], c, p.w, m.w, v.w, bc1, bc2, a.k);
+            __stcs(pm, p);
+            __stcs(mm, m);
+            __stcs(vv, v);
+            const uint2 w = make_uint2(narrow2<DT>(p.x, p.y), narrow2<DT>(p.z, p.w));
+            __stcs(reinterpret_cast<uint2*>(a.params) + vi, w);
+            widen2<DT>(w.x, x[0], x[1]);
+            widen2<DT>(w.y, x[2], x[3]);
+        }
+        quant_epilogue<QB, 4, ZERO_QBLOCK / 128>(x, vi << 2, live, a, sh_amax);
+        return;
+    }
     if (st.skipped || st.err) return;
     const float c = st.clip_coef, bc1 = st.bc1, bc2 = st.bc2;
     Unscale un;
@@ -248,8 +333,51 @@ __global__ void __launch_bounds__(ZERO_THREADS) k_update(const StepArgs a)
 
 // ---- fused single pass (no clip, no dynamic scale, no skip on overflow):
 // stages 1-6a ----------------------------------------------------------------
+// One 8-element vector of the step: fold, unscale, flag, squares, Adam, cast,
+// write-back; returns the 8 new 16-bit parameters packed in w.
 template <int DT, int ND>
-__global__ void __launch_bounds__(ZERO_THREADS) k_fused(const StepArgs a)
+static __device__ __forceinline__ void fused8(const StepArgs& a, int64_t vi, int nd,
+                                              const Unscale& un, float bc1, float bc2,
+                                              double& acc, int& bad, uint4& w)
+{
+    float4* pm = reinterpret_cast<float4*>(a.master);
+    float4* mm = reinterpret_cast<float4*>(a.m);
+    float4* vv = reinterpret_cast<float4*>(a.v);
+    float s[8], g[8], p[8], m[8], v[8];
+    const float4 p0 = __ldcs(pm + 2 * vi), p1 = __ldcs(pm + 2 * vi + 1);
+    const float4 m0 = __ldcs(mm + 2 * vi), m1 = __ldcs(mm + 2 * vi + 1);
+    const float4 v0 = __ldcs(vv + 2 * vi), v1 = __ldcs(vv + 2 * vi + 1);
+    fold8<DT, ND>(a.grads, a.rank_stride, vi, nd, s);
+#pragma unroll
+    for (int e = 0; e < 8; e++) {
+        g[e] = un(s[e]);
+        bad |= not_finite(g[e]);
+    }
+    acc += group_sumsq(g);
+    unpack8(p0, p1, p);
+    unpack8(m0, m1, m);
+    unpack8(v0, v1, v);
+#pragma unroll
+    for (int e = 0; e < 8; e++) adam1(g[e], 1.0f, p[e], m[e], v[e], bc1, bc2, a.k);
+    __stcs(pm + 2 * vi, make_float4(p[0], p[1], p[2], p[3]));
+    __stcs(pm + 2 * vi + 1, make_float4(p[4], p[5], p[6], p[7]));
+    __stcs(mm + 2 * vi, make_float4(m[0], m[1], m[2], m[3]));
+    __stcs(mm + 2 * vi + 1, make_float4(m[4], m[5], m[6], m[7]));
+    __stcs(vv + 2 * vi, make_float4(v[0], v[1], v[2], v[3]));
+    __stcs(vv + 2 * vi + 1, make_float4(v[4], v[5], v[6], v[7]));
+    w = make_uint4(narrow2<DT>(p[0], p[1]), narrow2<DT>(p[2], p[3]), narrow2<DT>(p[4], p[5]),
+                   narrow2<DT>(p[6], p[7]));
+    __stcs(reinterpret_cast<uint4*>(a.params) + vi, w);
+}
+
+// The fused pass.  QB = 8 or 4 adds the qwZ epilogue (ZeRO-3 shards only, whose
+// length is a multiple of 64): a warp's 32 vectors are 256 consecutive elements
+// starting on a multiple of 256, one quantization block, so the block's absmax
+// is one warp shuffle reduction.  The loop then runs while the warp's first
+// vector is in range, with the lanes past the end idle, so every lane takes the
+// shuffles.
+template <int DT, int ND, int QB>
+static __device__ __forceinline__ void fused_pass(const StepArgs& a)
 {
     __shared__ RedShared sh;
     const DevScalars sc = a.state->sc;
@@ -263,35 +391,27 @@ __global__ void __launch_bounds__(ZERO_THREADS) k_fused(const StepArgs a)
     int bad = 0;
     const int64_t nvec = a.n >> 3;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    float4* pm = reinterpret_cast<float4*>(a.master);
-    float4* mm = reinterpret_cast<float4*>(a.m);
-    float4* vv = reinterpret_cast<float4*>(a.v);
-    for (int64_t vi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; vi < nvec; vi += stride) {
-        float s[8], g[8], p[8], m[8], v[8];
-        const float4 p0 = __ldcs(pm + 2 * vi), p1 = __ldcs(pm + 2 * vi + 1);
-        const float4 m0 = __ldcs(mm + 2 * vi), m1 = __ldcs(mm + 2 * vi + 1);
-        const float4 v0 = __ldcs(vv + 2 * vi), v1 = __ldcs(vv + 2 * vi + 1);
-        fold8<DT, ND>(a.grads, a.rank_stride, vi, nd, s);
-#pragma unroll
-        for (int e = 0; e < 8; e++) {
-            g[e] = un(s[e]);
-            bad |= not_finite(g[e]);
+    if constexpr (QB == 0) {
+        for (int64_t vi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; vi < nvec; vi += stride) {
+            uint4 w;
+            fused8<DT, ND>(a, vi, nd, un, bc1, bc2, acc, bad, w);
         }
-        acc += group_sumsq(g);
-        unpack8(p0, p1, p);
-        unpack8(m0, m1, m);
-        unpack8(v0, v1, v);
-#pragma unroll
-        for (int e = 0; e < 8; e++) adam1(g[e], 1.0f, p[e], m[e], v[e], bc1, bc2, a.k);
-        __stcs(pm + 2 * vi, make_float4(p[0], p[1], p[2], p[3]));
-        __stcs(pm + 2 * vi + 1, make_float4(p[4], p[5], p[6], p[7]));
-        __stcs(mm + 2 * vi, make_float4(m[0], m[1], m[2], m[3]));
-        __stcs(mm + 2 * vi + 1, make_float4(m[4], m[5], m[6], m[7]));
-        __stcs(vv + 2 * vi, make_float4(v[0], v[1], v[2], v[3]));
-        __stcs(vv + 2 * vi + 1, make_float4(v[4], v[5], v[6], v[7]));
-        __stcs(reinterpret_cast<uint4*>(a.params) + vi,
-               make_uint4(narrow2<DT>(p[0], p[1]), narrow2<DT>(p[2], p[3]),
-                          narrow2<DT>(p[4], p[5]), narrow2<DT>(p[6], p[7])));
+    } else {
+        const int lane = threadIdx.x & 31;
+        for (int64_t vi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; vi - lane < nvec;
+             vi += stride) {
+            float x[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+            const bool live = vi < nvec;
+            if (live) {
+                uint4 w;
+                fused8<DT, ND>(a, vi, nd, un, bc1, bc2, acc, bad, w);
+                widen2<DT>(w.x, x[0], x[1]);
+                widen2<DT>(w.y, x[2], x[3]);
+                widen2<DT>(w.z, x[4], x[5]);
+                widen2<DT>(w.w, x[6], x[7]);
+            }
+            quant_epilogue<QB, 8, 1>(x, vi << 3, live, a, nullptr);
+        }
     }
     if (blockIdx.x == 0 && threadIdx.x < 8) {
         const int64_t i = (nvec << 3) + threadIdx.x;
@@ -308,6 +428,22 @@ __global__ void __launch_bounds__(ZERO_THREADS) k_fused(const StepArgs a)
         }
     }
     reduce_and_finalize(a, acc, bad, sh);
+}
+
+template <int DT, int ND>
+__global__ void __launch_bounds__(ZERO_THREADS) k_fused(const StepArgs a)
+{
+    fused_pass<DT, ND, 0>(a);
+}
+
+// The qwZ instances are held to 4 blocks per SM (64 registers; 2 for the
+// generic rank count), the occupancy the plain instances reach; unbounded, the
+// compiler keeps every rank's load of a vector in flight at once (254 registers,
+// one block per SM at nd 64).
+template <int DT, int ND, int QB>
+__global__ void __launch_bounds__(ZERO_THREADS, ND == 0 ? 2 : 4) k_fused_q(const StepArgs a)
+{
+    fused_pass<DT, ND, QB>(a);
 }
 
 }  // namespace zero

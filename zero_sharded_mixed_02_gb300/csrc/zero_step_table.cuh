@@ -29,6 +29,41 @@ static const void* fused_or_reduce(int kind)
     }
 }
 
+// The qwZ-epilogue instances (ZeRO-3 steps that also quantize the updated
+// shard), compiled in their own translation units.
+template <int DT, int ND>
+static const void* fused_or_update_q(int kind)
+{
+    switch (kind) {
+    case K_FUSED_Q8: return (const void*)k_fused_q<DT, ND, 8>;
+    case K_FUSED_Q4: return (const void*)k_fused_q<DT, ND, 4>;
+    case K_UPDATE_G32_Q8: return (const void*)k_update<DT, 0, false, 8>;
+    case K_UPDATE_G32_Q4: return (const void*)k_update<DT, 0, false, 4>;
+    case K_UPDATE_RECOMPUTE_Q8:
+        if constexpr (ND == 0 || ND < 4) return (const void*)k_update<DT, ND, true, 8>;
+        return nullptr;
+    case K_UPDATE_RECOMPUTE_Q4:
+        if constexpr (ND == 0 || ND < 4) return (const void*)k_update<DT, ND, true, 4>;
+        return nullptr;
+    default: return nullptr;
+    }
+}
+
+template <int DT>
+static const void* step_kernel_q_dt(int kind, int nd)
+{
+    switch (nd) {
+    case 1:  return fused_or_update_q<DT, 1>(kind);
+    case 2:  return fused_or_update_q<DT, 2>(kind);
+    case 4:  return fused_or_update_q<DT, 4>(kind);
+    case 8:  return fused_or_update_q<DT, 8>(kind);
+    case 16: return fused_or_update_q<DT, 16>(kind);
+    case 32: return fused_or_update_q<DT, 32>(kind);
+    case 64: return fused_or_update_q<DT, 64>(kind);
+    default: return fused_or_update_q<DT, 0>(kind);
+    }
+}
+
 template <int DT>
 static const void* step_kernel_dt(int kind, int nd)
 {
