@@ -90,8 +90,9 @@ CASES = [
 def test_bucketed_step_matches_oracle(env, case, bucket, reverse):
     torch, z = env
     gpu, padded = run_bucketed(torch, z, case, bucket, reverse)
-    ora = H.run_oracle(case, case.psi, padded)
+    ora = H.run_oracle(case, case.psi, padded, follow=gpu.results)
     H.compare_runs(gpu, ora, what=f"bucket={bucket}")
+    H.assert_state_equal(gpu, ora, what=f"bucket={bucket}")
     # the reduced gradient of the last step, bit for bit
     last = case.steps
     scale = gpu.results[-2]["loss_scale"] if last > 1 else case.loss_scale

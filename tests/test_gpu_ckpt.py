@@ -200,12 +200,15 @@ def run_steps(st, c, steps, scale):
     return out, scale
 
 
-def oracle_steps(c, steps, state, st_scalars):
+def oracle_steps(c, steps, state, st_scalars, follow=None):
+    """The oracle's steps; follow: the GPU's results of the same steps, whose
+    clip coefficients the oracle admits (harness.admit_clip)."""
     master, m, v, params = state
     res = []
-    for k in steps:
+    for i, k in enumerate(steps):
         g = np.ascontiguousarray(H.grads_for_step(c, k, c.psi, c.psi, st_scalars.loss_scale))
-        r = oracle.step(c.nd, c.dtype, g, master, m, v, params, c.opt(), st_scalars)
+        r = H.oracle_step_admitting(c.nd, c.dtype, g, master, m, v, params, c.opt(), st_scalars,
+                                    follow[i] if follow else None, what=f"step {k}")
         r["loss_scale"] = st_scalars.loss_scale
         r["t"] = st_scalars.t
         res.append(r)
@@ -312,7 +315,7 @@ def test_reshard_matches_oracle_and_continues(env, tmp_path, target):
     ostate = [flat_init(c), np.zeros(c.psi, np.float32), np.zeros(c.psi, np.float32),
               np.zeros(c.psi, np.uint16)]
     osc = oracle.new_scalars(c.loss_scale)
-    ores = oracle_steps(c, (1, 2, 3), ostate, osc)
+    ores = oracle_steps(c, (1, 2, 3), ostate, osc, follow=ra)
     assert [r["skipped"] for r in ores] == [r["skipped"] for r in ra] == [0, 1, 0]
 
     c2 = dataclasses.replace(c, **target)
@@ -345,7 +348,7 @@ def test_reshard_matches_oracle_and_continues(env, tmp_path, target):
         if c2.stage <= 2:
             # two more steps at the new rank count, against the oracle doing the same
             rb, _ = run_steps(b, c2, (4, 5), scale)
-            ores2 = oracle_steps(c2, (4, 5), ostate, osc)
+            ores2 = oracle_steps(c2, (4, 5), ostate, osc, follow=rb)
             H.compare_runs(H.Run(*flat_of(c2, b.host()), rb), H.Run(*ostate, ores2),
                            what=f"after reshard to {target}")
     finally:

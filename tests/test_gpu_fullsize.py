@@ -97,23 +97,25 @@ def test_gpt2_1p5b_nd16_full_schedule(z):
                 assert not ovf
             c = oracle.clip_coef(norm, w.clip)
             res = oracle.advance(opt, st, ovf)
+            if not res.skipped:
+                c_used = H.admit_clip(c, r, f"step {step}")
             skips.append(r["skipped"])
             assert r["skipped"] == res.skipped == int(inject), f"step {step}"
             assert z.zero_step_overflow(plan) == int(ovf)
             assert (r["t"], r["loss_scale"]) == (st.t, st.loss_scale), f"step {step}"
             if not res.skipped:
                 assert abs(r["grad_norm"] - norm) <= H.REL_NORM * norm, f"step {step}"
-                assert abs(r["clip_coef"] - c) <= 4e-7 * c, f"step {step}"
+                assert H.ulps32(r["clip_coef"], c) <= H.CLIP_ULPS, f"step {step}"
                 g16 = H.oracle_sampled_grads(w.seed, step, w.nd, idx, w.grad_sigma, scale, w.dtype)
                 g, _ = oracle.reduce(w.nd, w.dtype, g16, loss_scale=scale)
                 # the reduced gradient in the workspace is bit-exact at every sample
                 assert np.array_equal(at(work, idx_t).view(np.uint32), g.view(np.uint32))
-                oracle.adam(g, c, ms, mm, vs, ps, w.dtype, opt, res.bc1, res.bc2)
+                oracle.adam(g, c_used, ms, mm, vs, ps, w.dtype, opt, res.bc1, res.bc2)
             else:
                 assert not np.isfinite(r["grad_norm"])
-            H.assert_state_close((at(master, idx_t), at(m, idx_t), at(v, idx_t),
-                                  at(params, idx_t).view(np.uint16)), (ms, mm, vs, ps),
-                                 f"gpt2-1.5b step {step}")
+            for x, y in zip((at(master, idx_t), at(m, idx_t), at(v, idx_t)), (ms, mm, vs)):
+                assert np.array_equal(x.view(np.uint32), y.view(np.uint32)), f"step {step}"
+            assert np.array_equal(at(params, idx_t).view(np.uint16), ps), f"step {step}"
             scale = st.loss_scale
         assert skips == [0, 0, 1, 0, 0, 0, 1, 0, 0, 0]
         assert (st.t, st.loss_scale) == (8, 16384.0)
@@ -123,14 +125,15 @@ def test_gpt2_1p5b_nd16_full_schedule(z):
 
 def test_gpt2_small_nd8_full_size_all_elements(z):
     """GPT-2 small, Nd = 8, ZeRO-1, bf16, AdamW 0.01, clip 1.0, 10 steps: every
-    element of every output against the sharded oracle."""
+    element of every output bit for bit against the oracle (which admits the
+    GPU's clip coefficient when it is within the harness's bound of its own)."""
     import torch
     w = W.gpt2_small()
     dev = torch.device("cuda", 0)
     sp = torch.cuda.current_stream().cuda_stream
     plan = z.zero_plan_create(w.psi, w.nd, w.stage, w.dtype, w.shapes, hp_of(z, w))
     try:
-        shard, padded, _, ws = z.zero_plan_layout(plan)
+        _, padded, _, ws = z.zero_plan_layout(plan)
         grads = torch.empty((w.nd, padded), dtype=torch.int16, device=dev)
         master = torch.zeros(padded, dtype=torch.float32, device=dev)
         m, v = torch.zeros_like(master), torch.zeros_like(master)
@@ -149,17 +152,17 @@ def test_gpt2_small_nd8_full_size_all_elements(z):
             r = z.zero_step_result(plan)
             g16 = gen.ranks_16_mt(w.seed, gen.STREAM_GRAD, step, w.nd, w.psi, w.grad_sigma, 1.0,
                                   w.dtype)
-            ro = oracle.step_sharded(w.nd, w.dtype, g16, om, omm, ov, op, opt, st,
-                                     shard=shard, nthreads=w.nd)
+            ro = H.oracle_step_admitting(w.nd, w.dtype, g16, om, omm, ov, op, opt, st, r,
+                                         what=f"step {step}")
             del g16
             assert r["t"] == st.t and r["skipped"] == ro["skipped"] == 0
             assert abs(r["grad_norm"] - ro["grad_norm"]) <= H.REL_NORM * ro["grad_norm"]
             assert r["clip_coef"] < 1.0
         torch.cuda.synchronize()
-        H.assert_state_close((master[:w.psi].cpu().numpy(), m[:w.psi].cpu().numpy(),
-                              v[:w.psi].cpu().numpy(),
-                              params[:w.psi].cpu().numpy().view(np.uint16)), (om, omm, ov, op),
-                             "gpt2-small")
+        H.assert_state_equal(H.Run(master[:w.psi].cpu().numpy(), m[:w.psi].cpu().numpy(),
+                                   v[:w.psi].cpu().numpy(),
+                                   params[:w.psi].cpu().numpy().view(np.uint16), []),
+                             H.Run(om, omm, ov, op, []), "gpt2-small")
     finally:
         z.zero_plan_destroy(plan)
 

@@ -59,7 +59,9 @@ def run_offload(torch, z, c, nthreads=0):
         z.zero_plan_destroy(plan)
 
 
-def run_oracle_offload(c):
+def run_oracle_offload(c, follow=None):
+    """The oracle's offloaded steps; follow: the GPU's per-step results, whose
+    clip coefficients it admits (harness.admit_clip)."""
     n = c.psi
     state = [gen.f32(c.seed, gen.STREAM_MASTER, 0, 0, n, 0.02), np.zeros(n, np.float32),
              np.zeros(n, np.float32), np.zeros(n, np.uint16)]
@@ -67,7 +69,11 @@ def run_oracle_offload(c):
     res = []
     for step in range(1, c.steps + 1):
         g = np.ascontiguousarray(H.grads_for_step(c, step, n, n, st.loss_scale))
-        r = oracle.step_offload(c.nd, c.dtype, g, *state, c.opt(), st)
+        if follow is None:
+            r = oracle.step_offload(c.nd, c.dtype, g, *state, c.opt(), st)
+        else:
+            r = H.oracle_step_admitting(c.nd, c.dtype, g, *state, c.opt(), st, follow[step - 1],
+                                        offload=True, what=f"step {step}")
         r["loss_scale"] = st.loss_scale
         r["t"] = st.t
         res.append(r)
@@ -88,7 +94,7 @@ CASES = [
 def test_offload_step_matches_oracle(env, c):
     torch, z = env
     gpu, g16, (g_last, s_last) = run_offload(torch, z, c)
-    ora = run_oracle_offload(c)
+    ora = run_oracle_offload(c, follow=gpu.results)
     H.compare_runs(gpu, ora, what="offload")
     want16, _, _ = oracle.reduce16(c.nd, c.dtype, np.ascontiguousarray(g_last[:, :c.psi]),
                                    loss_scale=s_last)
@@ -137,5 +143,6 @@ def test_gpt2_small_full_size(env):
     torch, z = env
     c = H.from_workload(W.gpt2_small(), steps=2)
     gpu, _, _ = run_offload(torch, z, c)
-    ora = run_oracle_offload(c)
+    ora = run_oracle_offload(c, follow=gpu.results)
     H.compare_runs(gpu, ora, what="GPT-2 small offload")
+    H.assert_state_equal(gpu, ora, what="GPT-2 small offload")

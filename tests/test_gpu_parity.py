@@ -26,7 +26,10 @@ def z():
     return z
 
 
-def check(z, c, bit_exact=False, g32=False, reduce_kernel=0):
+def check(z, c, g32=False, reduce_kernel=0):
+    """The case through the library and through the oracle (which admits the
+    GPU's clip coefficient when it is within the harness's bound of its own);
+    results by the harness's rules and the state bit for bit."""
     gpu = H.run_gpu(z, c, keep_g32=g32, reduce_kernel=reduce_kernel)
     n = gpu.master.size
     padded = n
@@ -39,12 +42,9 @@ def check(z, c, bit_exact=False, g32=False, reduce_kernel=0):
         plan = z.zero_plan_create(c.psi, c.nd, 3, c.dtype, c.shapes, c.hparams(z), units=c.units)
         mask = H.stage3_valid_mask(z, plan, c.nd)
         z.zero_plan_destroy(plan)
-    ora = H.run_oracle(c, n, padded, mask)
+    ora = H.run_oracle(c, n, padded, mask, follow=gpu.results)
     H.compare_runs(gpu, ora, what=f"psi={c.psi} nd={c.nd}")
-    if bit_exact:
-        for a, b in zip((gpu.master, gpu.m, gpu.v, gpu.params), (ora.master, ora.m, ora.v, ora.params)):
-            assert np.array_equal(a.view(np.uint32 if a.dtype == np.float32 else np.uint16),
-                                  b.view(np.uint32 if b.dtype == np.float32 else np.uint16))
+    H.assert_state_equal(gpu, ora, what=f"psi={c.psi} nd={c.nd}")
     if g32:
         # the reduced (averaged, unscaled) gradient of the last step is bit-exact
         last = c.steps
@@ -58,7 +58,7 @@ def check(z, c, bit_exact=False, g32=False, reduce_kernel=0):
 def test_tiny_flat_model(z):
     # tiny flat model: 4 tensors, Nd=4, ZeRO-2, fp16 x1024 dynamic loss scale, 3 steps
     c = H.from_workload(W.tiny())
-    gpu, ora = check(z, c, bit_exact=True, g32=True)
+    gpu, ora = check(z, c, g32=True)
     assert [r["t"] for r in gpu.results] == [1, 2, 3]
 
 
@@ -95,8 +95,9 @@ def test_llama_family_stage3_and_gather(z):
         _, total, nunits, _ = z.zero_plan_layout(plan)
         assert nunits == 4
         mask = H.stage3_valid_mask(z, plan, c.nd)
-        ora = H.run_oracle(c, total, total, mask)
+        ora = H.run_oracle(c, total, total, mask, follow=gpu.results)
         H.compare_runs(gpu, ora, "stage3")
+        H.assert_state_equal(gpu, ora, "stage3")
         dev = torch.device("cuda", 0)
         shards = [torch.from_numpy(gpu.params.view(np.int16)).to(dev)]
         host_shards = [gpu.params]
@@ -123,7 +124,7 @@ def test_bandwidth_sweep_point(z, nd):
     # the sweep's flat bf16 model (no clip, no loss scale: the fused single pass),
     # 5 warm-up steps + 1; every output bit-exact
     c = H.Case(shapes=[(1 << 20,)], nd=nd, steps=6)
-    check(z, c, bit_exact=True)
+    check(z, c)
 
 
 EDGE = []
@@ -143,14 +144,14 @@ def test_edge_sizes(z, psi, nd, mode):
     else:
         c = H.Case(shapes=shapes, nd=nd, steps=4, dtype=gen.FP16, grad_sigma=1e-3,
                    loss_scale=4096.0, dynamic_scale=1, inf_steps=(2,), growth_interval=2)
-    check(z, c, bit_exact=(mode != "clip"), g32=(mode != "fused" and nd >= 4))
+    check(z, c, g32=(mode != "fused" and nd >= 4))
 
 
 def test_nan_and_inf_skip_and_scale_schedule(z):
     c = H.Case(shapes=[(3000,), (1000,)], nd=4, dtype=gen.FP16, grad_sigma=1e-3,
                loss_scale=1024.0, dynamic_scale=1, steps=7, inf_steps=(2,), nan_steps=(5,),
                growth_interval=2)
-    gpu, _ = check(z, c, bit_exact=True)
+    gpu, _ = check(z, c)
     assert [r["skipped"] for r in gpu.results] == [0, 1, 0, 0, 1, 0, 0]
     assert [r["loss_scale"] for r in gpu.results] == [1024, 512, 512, 1024, 512, 512, 1024]
 
@@ -175,8 +176,7 @@ def test_static_scale_overflow_against_the_oracle(z, name):
     reported and the step goes ahead (no clip: only the planted element turns
     non-finite; clip: tau / inf = 0 makes every other element take a
     zero-gradient step); with it the step is skipped and the scale kept.  +inf
-    at step 2, NaN at step 4, 5 steps; without a clip every other element is
-    bit-exact, with one within the state tolerances."""
+    at step 2, NaN at step 4, 5 steps; every other element bit-exact."""
     over, path = STATIC_OVERFLOW[name]
     c = H.Case(shapes=[(40_000,), (1_003,)], steps=5, inf_steps=(2,), nan_steps=(4,), **over)
     plan = z.zero_plan_create(c.psi, c.nd, c.stage, c.dtype, c.shapes, c.hparams(z))
@@ -192,11 +192,6 @@ def test_static_scale_overflow_against_the_oracle(z, name):
     assert bad.any() == (not skip) and np.array_equal(bad, np.isnan(gpu.master))
     if not skip and not c.clip:
         assert bad.sum() == 2                      # the two planted elements only
-    if not c.clip:           # with a clip, c may differ in its last bit (the norm's rounding)
-        for a, b in zip((gpu.master, gpu.m, gpu.v), (ora.master, ora.m, ora.v)):
-            keep = ~(np.isnan(a) & np.isnan(b))
-            assert np.array_equal(a[keep].view(np.uint32), b[keep].view(np.uint32))
-        assert np.array_equal(gpu.params[~bad], ora.params[~bad])
 
 
 def test_empty_model(z):
@@ -336,7 +331,7 @@ def test_largest_rank_counts(z, nd, mode):
     else:
         c = H.Case(shapes=shapes, nd=nd, steps=3, dtype=gen.FP16, grad_sigma=1e-3,
                    loss_scale=4096.0, dynamic_scale=1, inf_steps=(2,))
-    gpu, _ = check(z, c, bit_exact=(mode != "clip"), g32=True)
+    gpu, _ = check(z, c, g32=True)
     if mode != "clip":
         assert [r["skipped"] for r in gpu.results] == [0, 1, 0]
 
@@ -356,8 +351,9 @@ def test_largest_rank_count_stage3_gathers(z):
         _, total, nunits, _ = z.zero_plan_layout(plan)
         assert nunits == 2
         mask = H.stage3_valid_mask(z, plan, nd)
-        ora = H.run_oracle(c, total, total, mask)
+        ora = H.run_oracle(c, total, total, mask, follow=gpu.results)
         H.compare_runs(gpu, ora, "stage3 nd=1000")
+        H.assert_state_equal(gpu, ora, "stage3 nd=1000")
         dev = torch.device("cuda", 0)
         sp = torch.cuda.current_stream().cuda_stream
         host_shards = [gpu.params]
@@ -409,7 +405,7 @@ def test_degenerate_settings(z, name, kernels):
     # without it, bit for bit.
     kw = DEGENERATE[name]
     c = H.Case(shapes=[(50_003,), (5,)], nd=4, steps=3, **kw)
-    gpu, _ = check(z, c, bit_exact=not kw.get("clip"), reduce_kernel=kernels)
+    gpu, _ = check(z, c, reduce_kernel=kernels)
     if name == "lr-zero":
         master0 = gen.f32(c.seed, gen.STREAM_MASTER, 0, 0, c.psi, 0.02)
         assert gpu.master.tobytes() == master0.tobytes()
@@ -433,6 +429,6 @@ def test_stage3_modes(z, nd, mode):
         c = H.Case(shapes=shapes, nd=nd, stage=3, units=units, steps=4, dtype=gen.FP16,
                    grad_sigma=1e-3, loss_scale=4096.0, dynamic_scale=1, inf_steps=(2,),
                    growth_interval=2)
-    gpu, _ = check(z, c, bit_exact=(mode != "clip"))
+    gpu, _ = check(z, c)
     if mode == "fp16-dyn":
         assert [r["skipped"] for r in gpu.results] == [0, 1, 0, 0]

@@ -131,9 +131,10 @@ def test_step_qwz_against_oracle_and_zero_step(env, name, bits):
 
 @pytest.mark.parametrize("bits", [8, 4])
 def test_step_qwz_with_clip_matches_the_standalone_quantizer(env, bits):
-    """With a clip the clip coefficient may differ from the oracle's in its last
-    bit, so the codes are checked against zero_quantize_shard of the same updated
-    shard, and the state against the oracle within the parity tolerances."""
+    """With a clip, the oracle admits the GPU's clip coefficient (the harness's
+    rule); the state is then the oracle's bit for bit, and the codes are checked
+    against zero_quantize_shard of the same updated shard and against the
+    oracle's quantizer on the oracle's shard."""
     torch, z = env
     c = H.Case(steps=3, stage=3, nd=8, dtype=gen.BF16, clip=0.05, **LARGE)
     per_step, (qa, _), L, mask = run_both(torch, z, c, bits)
@@ -145,8 +146,11 @@ def test_step_qwz_with_clip_matches_the_standalone_quantizer(env, bits):
     torch.cuda.synchronize()
     assert np.array_equal(per_step[-1][0], codes.cpu().numpy())
     assert np.array_equal(per_step[-1][1].view(np.uint32), scales.cpu().numpy().view(np.uint32))
-    ora = H.run_oracle(c, L, L, mask)
-    H.assert_state_close(qa, (ora.master, ora.m, ora.v, ora.params), "clip")
+    ora = H.run_oracle(c, L, L, mask, follow=[r for _, _, r in per_step])
+    H.assert_state_equal(H.Run(*qa, []), ora, "clip")
+    q, s = oracle.quantize_16(c.dtype, ora.params, bits, 256)
+    assert np.array_equal(per_step[-1][0], q)
+    assert np.array_equal(per_step[-1][1].view(np.uint32), s.view(np.uint32))
 
 
 def test_step_qwz_rejects_bad_arguments(env):
