@@ -89,7 +89,7 @@ def measured_peaks():
 
 
 KERNEL_SOURCES = ("zero_common.cuh", "zero_step_kernels.cuh", "zero_step_table.cuh",
-                  "zero_step_fp16.cu", "zero_step_bf16.cu", "zero_tma.cuh")
+                  "zero_step_fp16.cu", "zero_step_bf16.cu", "zero_tma.cuh", "zero_qwz.cuh")
 
 
 def kernel_source_sha() -> str:
@@ -195,6 +195,21 @@ class HugePinned:
             self.map.close()
         except BufferError:          # a view is still alive: the mapping goes with it
             pass
+
+
+def huge_host_array(n: int, dtype):
+    """A host numpy array of n elements in anonymous memory advised to use
+    transparent huge pages (MADV_HUGEPAGE), zero-filled: host state arrays of tens
+    of GB otherwise sit on small pages.  The mapping lives as long as the array."""
+    import mmap
+    import numpy as np
+    nbytes = max(1, n * np.dtype(dtype).itemsize)
+    mp = mmap.mmap(-1, nbytes, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
+    try:
+        mp.madvise(mmap.MADV_HUGEPAGE)
+    except (AttributeError, OSError):
+        pass
+    return np.frombuffer(mp, dtype=dtype, count=n)
 
 
 def pinning_fits(nbytes: int, device=None, avail=None):
@@ -1030,11 +1045,13 @@ def run_checkpoint(args):
 
 def host_copy_gbs(threads, nbytes=4 << 30):
     """Host memory bandwidth for scale: `threads` threads each copying their slice
-    of an nbytes array (numpy copies release the GIL); read + write bytes / s."""
+    of an nbytes array (numpy copies release the GIL); read + write bytes / s.
+    The arrays sit on transparent huge pages, like the offload leg's host state."""
     import numpy as np
     from concurrent.futures import ThreadPoolExecutor
-    src = np.ones(nbytes // 4, np.float32)
-    dst = np.empty_like(src)
+    src = huge_host_array(nbytes // 4, np.float32)
+    src[:] = 1.0
+    dst = huge_host_array(nbytes // 4, np.float32)
     parts = np.array_split(np.arange(src.size), threads)
     bounds = [(int(p[0]), int(p[-1]) + 1) for p in parts if p.size]
 
@@ -1075,10 +1092,13 @@ def run_offload(args):
         n = w.psi
         d = torch.zeros(padded, dtype=torch.float32, device=dev)
         gen.cuda_f32(d.data_ptr(), 0, gen.STREAM_MASTER, 0, 0, n, 0.02)
-        master = d.cpu().numpy()
+        # host state on transparent huge pages (the host Adam streams 28 bytes
+        # per parameter through these arrays every step)
+        master = huge_host_array(padded, np.float32)
+        master[:] = d.cpu().numpy()
         del d
-        m = np.zeros(padded, np.float32)
-        v = np.zeros(padded, np.float32)
+        m = huge_host_array(padded, np.float32)
+        v = huge_host_array(padded, np.float32)
         params = torch.zeros(padded, dtype=torch.int16, device=dev)
         work = torch.empty(padded, dtype=torch.int16, device=dev)
         grads = torch.empty((w.nd, padded), dtype=torch.int16, device=dev)
@@ -1095,8 +1115,9 @@ def run_offload(args):
         t_step = (time.perf_counter() - t0) / K
         r = z.zero_step_result(plan)
         # the host Adam alone, on the last copied gradient
-        g16 = work[:n].cpu().numpy()
-        p16 = np.empty(n, np.uint16)
+        g16 = huge_host_array(n, np.uint16)
+        g16[:] = work[:n].cpu().numpy()
+        p16 = huge_host_array(n, np.uint16)
         hp = z.hparams(**w.hparams())
         z.zero_cpu_adam(g16, w.dtype, n, r["loss_scale"], 1.0, 0.5, 0.5, hp, master, m, v,
                         p16, threads)

@@ -19,8 +19,8 @@ namespace {
 constexpr int PATH_FUSED = 0, PATH_G32 = 1, PATH_RECOMPUTE = 2;
 constexpr int PROFILE_RING = 256;
 constexpr uint64_t LAYOUT_ALIGN = 64;   // elements; keeps 16-byte vectors inside a shard
-constexpr uint64_t REDUCE_WAVES = 12;   // reduce grid: waves of SMs x occupancy (measured)
-constexpr uint64_t FUSED_WAVES = 8;     // fused single-pass grid
+constexpr uint64_t REDUCE_WAVES = 12;   // reduce grid: at most this many waves (measured)
+constexpr uint64_t FUSED_WAVES = 8;     // fused single-pass grid: at most this many waves
 constexpr uint64_t TMA_STAGE_BUDGET = 131072;  // bytes of staged rows per CTA (4 stages at nd 16)
 constexpr uint64_t TMA_SMEM_MAX = 196608;      // largest ring of stages a CTA may hold
 
@@ -126,17 +126,28 @@ void destroy_plan(zero_plan* p)
     delete p;
 }
 
-// Reduce and fused passes: `waves` waves of (SMs x resident blocks per SM),
-// capped by the work (one thread per 8-element vector) and by the per-block
-// partials array.
-int grid_reduce(const void* fn, int sms, uint64_t n, uint64_t waves)
+// Reduce and fused passes: a whole number of waves of (SMs x resident blocks per
+// SM), at most max_waves, and no more waves than leave every thread at least
+// MIN_VECTORS_PER_THREAD of its 8-element vectors; capped by the work (one
+// thread per vector) and by the per-block partials array.  Measured on the
+// fused pass: more waves are faster while a thread keeps about six vectors or
+// more (2^26-2^31 elements: 8 waves, 0.94-1.07 of the copy rate, against
+// 0.89-1.05 for 1-3), and slower below that (2^24 elements: 2 waves, 0.85-1.02,
+// against 0.74-0.97 for 8, where a thread has two or three vectors and the
+// last round runs a third full).
+constexpr uint64_t MIN_VECTORS_PER_THREAD = 6;
+int grid_reduce(const void* fn, int sms, uint64_t n, uint64_t max_waves)
 {
     int occ = 1;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, ZERO_THREADS, 0) != cudaSuccess ||
         occ < 1)
         occ = 1;
-    const uint64_t want = std::max<uint64_t>(1, ceil_div(n / 8, ZERO_THREADS));
-    uint64_t g = std::min<uint64_t>((uint64_t)sms * (uint64_t)occ * waves, want);
+    const uint64_t nvec = n / 8;
+    const uint64_t per_wave = (uint64_t)sms * (uint64_t)occ;
+    const uint64_t waves = std::min<uint64_t>(
+        max_waves, std::max<uint64_t>(1, nvec / (per_wave * ZERO_THREADS * MIN_VECTORS_PER_THREAD)));
+    const uint64_t want = std::max<uint64_t>(1, ceil_div(nvec, ZERO_THREADS));
+    uint64_t g = std::min<uint64_t>(per_wave * waves, want);
     g = std::min<uint64_t>(g, ZERO_MAX_BLOCKS);
     return (int)std::max<uint64_t>(g, 1);
 }

@@ -119,7 +119,9 @@ __global__ void __launch_bounds__(ZERO_THREADS, 3) k_quantize(const uint16_t* __
 // 256-element scale block (unit offsets are multiples of 64).  The thread whose
 // 8 outputs run past the valid part takes them element by element.  QG = 2 at 8
 // bits and 4 at 4 bits: at 4 bits a group loads only 4 bytes of codes, and two
-// groups per thread left too few loads in flight.
+// groups per thread left too few loads in flight.  The 4-bit decode makes each
+// code a float by exponent-field arithmetic rather than an integer conversion
+// (measured: 3.46 -> 3.08 ms for LLaMA-3-8B's 34 unit gathers at Nd = 64).
 template <int BITS> struct Qg { static constexpr int v = BITS == 8 ? 2 : 4; };
 
 static __device__ __forceinline__ int32_t code_at(const uint8_t* codes, int64_t e, int bits)
@@ -160,21 +162,34 @@ __global__ void __launch_bounds__(ZERO_THREADS) k_gather_q(const __grid_constant
             }
         }
     }
+    // keep every load above ahead of the decode below: left to itself the
+    // compiler sinks them into the decode loop, and fewer are in flight
+    asm volatile("" ::: "memory");
 #pragma unroll
     for (int g = 0; g < QG; g++) {
         const int64_t j = j0 + g * 8 * ZERO_THREADS;
         if (j + 8 <= valid) {
             float f[8];
+            if (BITS == 8) {
 #pragma unroll
-            for (int i = 0; i < 8; i++) {
-                int32_t c;
-                if (BITS == 8) {
-                    c = (int8_t)(word[g][i / 4] >> (8 * (i % 4)));
-                } else {
-                    c = (int32_t)((word[g][0] >> (4 * i)) & 0xF);
-                    c = c >= 8 ? c - 16 : c;
+                for (int i = 0; i < 8; i++) {
+                    const int32_t c = (int8_t)(word[g][i / 4] >> (8 * (i % 4)));
+                    f[i] = __fmul_rn((float)c, s[g]);
                 }
-                f[i] = __fmul_rn((float)c, s[g]);
+            } else {
+                // 4-bit code c (two's complement nibble q): q ^ 8 = c + 8, and the
+                // binary32 with exponent field 150 and that value in its mantissa
+                // is 2^23 + c + 8 exactly, so one subtraction of 2^23 + 8 gives c
+                // as a float without an integer conversion; then the product c *
+                // scale, rounded once as before (on packed pairs).
+                const f32x2_t bias = pack2(8388616.0f, 8388616.0f), s2 = pack2(s[g], s[g]);
+#pragma unroll
+                for (int i = 0; i < 8; i += 2) {
+                    const uint32_t w = word[g][0] >> (4 * i);
+                    const float a0 = __uint_as_float(((w & 0xFu) ^ 8u) | 0x4B000000u);
+                    const float a1 = __uint_as_float((((w >> 4) & 0xFu) ^ 8u) | 0x4B000000u);
+                    unpack2(mul2(sub2(pack2(a0, a1), bias), s2), f[i], f[i + 1]);
+                }
             }
             __stcs(reinterpret_cast<uint4*>(a.out + base + j),
                    make_uint4(narrow2<DT>(f[0], f[1]), narrow2<DT>(f[2], f[3]),
