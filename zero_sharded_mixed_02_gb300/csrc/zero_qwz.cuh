@@ -74,15 +74,6 @@ static __device__ __forceinline__ float max_nan(float a, float b)
     return r;
 }
 
-// t = fl(v * r) rounded to an integer by adding 1.5 * 2^23 (u holds the sum);
-// true when t lies within 2^-14 of a half-integer, or is NaN.
-static __device__ __forceinline__ bool near_half(float v, float r, float* u)
-{
-    const float t = __fmul_rn(v, r);
-    *u = __fadd_rn(t, ZERO_RND);
-    return !(fabsf(__fsub_rn(t, __fsub_rn(*u, ZERO_RND))) <= 0.5f - 0x1p-14f);
-}
-
 // The codes of N elements (N even) of one block: each is the integer nearest to
 // fl(v / scale) (ties to even), clamped to [-qmax, qmax]; returned as words whose
 // low bits hold the two's-complement code.
@@ -112,24 +103,26 @@ static __device__ __forceinline__ void codes_n(const float* v, float scale, uint
     const float r = __fmaf_rn(__fmaf_rn(-scale, r0, 1.0f), r0, r0);
     const f32x2_t r2 = pack2(r, r), rnd2 = pack2(ZERO_RND, ZERO_RND);
     float dmax = 0.0f;
+    float d[N];                                       // t minus its rounded integer
 #pragma unroll
-    for (int i = 0; i < N; i += 2) {                  // near_half, two lanes at a time
+    for (int i = 0; i < N; i += 2) {                  // two lanes at a time
         const f32x2_t t = mul2(pack2(v[i], v[i + 1]), r2);
         const f32x2_t u = add2(t, rnd2);
-        float d0, d1, u0, u1;
-        unpack2(sub2(t, sub2(u, rnd2)), d0, d1);
-        dmax = max_nan(dmax, fabsf(d0));
-        dmax = max_nan(dmax, fabsf(d1));
+        float u0, u1;
+        unpack2(sub2(t, sub2(u, rnd2)), d[i], d[i + 1]);
+        dmax = max_nan(dmax, fabsf(d[i]));
+        dmax = max_nan(dmax, fabsf(d[i + 1]));
         unpack2(u, u0, u1);
         c[i] = __float_as_uint(u0);
         c[i + 1] = __float_as_uint(u1);
     }
+    // the elements within 2^-14 of a half-integer (or NaN) take the exact quotient;
+    // their residuals are kept from above rather than recomputed (measured: the
+    // standalone quantizer 82 -> 74 us on a 120 M-element bf16 shard)
     if (!(dmax <= 0.5f - 0x1p-14f)) {
 #pragma unroll
-        for (int i = 0; i < N; i++) {
-            float u;
-            if (near_half(v[i], r, &u)) c[i] = (uint32_t)quant1(v[i], scale, qmax);
-        }
+        for (int i = 0; i < N; i++)
+            if (!(fabsf(d[i]) <= 0.5f - 0x1p-14f)) c[i] = (uint32_t)quant1(v[i], scale, qmax);
     }
 }
 
