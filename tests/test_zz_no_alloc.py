@@ -108,6 +108,32 @@ def test_overflow_flag_then_clean_call(env):
     assert abs(got_norm - want_norm) <= H.REL_NORM * want_norm
 
 
+def test_calls_take_no_device_memory(env):
+    """After one call per 16-bit format (which may load the kernels and the scratch
+    array's module on first use), further calls leave the device's free memory
+    unchanged: the entry point allocates nothing (any device allocation takes at
+    least a page of the device's free memory)."""
+    torch, z = env
+    dev = torch.device("cuda", 0)
+    nd, psi = 4, 600_001
+    bufs = {}
+    for dtype in (gen.FP16, gen.BF16):
+        g, padded = grads(nd, psi, dtype, 1e-3, 64.0, step=5)
+        bufs[dtype] = (torch.from_numpy(g.view(np.int16)).to(dev), padded)
+    norm = torch.zeros(1, dtype=torch.float64, device=dev)
+    ovf = torch.zeros(1, dtype=torch.int32, device=dev)
+    sp = torch.cuda.current_stream().cuda_stream
+    for dtype, (g, padded) in bufs.items():                 # first calls: lazy loading
+        z.zero_grad_norm_noalloc(g, nd, psi, padded, dtype, 64.0, norm, ovf, sp)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(20):
+        for dtype, (g, padded) in bufs.items():
+            z.zero_grad_norm_noalloc(g, nd, psi, padded, dtype, 64.0, norm, ovf, sp)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+
+
 def test_sizes_beyond_the_scratch_are_rejected(env):
     torch, z = env
     out = torch.zeros(2, dtype=torch.float64, device="cuda")

@@ -151,6 +151,11 @@ __global__ void __launch_bounds__(ZERO_THREADS, 4) k_reduce(const StepArgs a)
     // the update pass may be scheduled now: it loads its state, then waits for
     // this grid to finish before it reads anything this grid writes
     asm volatile("griddepcontrol.launch_dependents;");
+    // a bucket's reduce is launched as a programmatic dependent of whatever the
+    // stream ran before it (so its blocks are placed during the previous grid's
+    // tail): it reads nothing until that grid has completed and its writes are
+    // visible, whoever wrote the bucket's gradients
+    if (a.bucket >= 0) asm volatile("griddepcontrol.wait;" ::: "memory");
     const int nd = ND > 0 ? ND : a.nd;
     Unscale un;
     un.init(nd, a.state->sc.loss_scale);
