@@ -234,7 +234,8 @@ zero_status_t zero_gather_layer(zero_plan_t plan, int unit, const void* const* s
  *   zero_plan_set_bucket   turns bucketed steps on (B > 0) or off (B = 0) and
  *                          reports the workspace they need: the fp32 reduced
  *                          gradient (n floats) plus one norm partial and one
- *                          flag per bucket.  Waits for the plan's last step.
+ *                          flag per block of each bucket's reduce.  Waits for
+ *                          the plan's last step.
  *   zero_step_bucket       reduces bucket b: bucket_grads is [nd][B] 16-bit
  *                          (rank stride B; a short last bucket uses its first
  *                          count columns); buckets may come in any order, each
@@ -242,9 +243,10 @@ zero_status_t zero_gather_layer(zero_plan_t plan, int unit, const void* const* s
  *                          bucket buffer may be reused once this call's work
  *                          on `stream` is done.
  *   zero_step_apply        after every bucket: the global norm from the bucket
- *                          partials (summed in bucket order), clip, skip
- *                          decision, Adam, cast, write-back; ZERO_EINVAL if a
- *                          bucket is missing.  zero_step_result reports it.
+ *                          reduces' block partials (summed in bucket, then
+ *                          block, order), clip, skip decision, Adam, cast,
+ *                          write-back; ZERO_EINVAL if a bucket is missing.
+ *                          zero_step_result reports it.
  * Reduced gradients are bit-identical to zero_step's; the norm agrees to
  * 1e-5 (its partial sums are grouped by bucket).  Calls of one plan must be
  * ordered on one stream. */

@@ -44,7 +44,10 @@ def run_bucketed(torch, z, c, bucket_elems, reverse=True):
         results, scale = [], c.loss_scale
         order = list(range(nb))[::-1] if reverse else list(range(nb))
         for step in range(1, c.steps + 1):
-            site = gen.inf_site(c.seed, step, n, c.nd) if step in c.inf_steps else None
+            # +inf / NaN at the same site harness.grads_for_step plants them
+            bits = (0x7C00 if c.dtype == gen.FP16 else 0x7F80) if step in c.inf_steps else \
+                   (0x7E00 if c.dtype == gen.FP16 else 0x7FC0) if step in c.nan_steps else None
+            site = gen.inf_site(c.seed, step, n, c.nd) if bits is not None else None
             for j, b in enumerate(order):
                 buf = bufs[j % 2]
                 first, count = b * bucket_elems, min(bucket_elems, n - b * bucket_elems)
@@ -55,7 +58,7 @@ def run_bucketed(torch, z, c, bucket_elems, reverse=True):
                                       c.grad_sigma, scale, c.dtype, rank_stride=bucket_elems,
                                       index0=first, cuda_stream=producer.cuda_stream)
                     if site and first <= site[1] < first + count:
-                        buf[site[0], site[1] - first] = 0x7C00 if c.dtype == gen.FP16 else 0x7F80
+                        buf[site[0], site[1] - first] = bits
                     ready = torch.cuda.Event()
                     ready.record(producer)
                 consumer.wait_event(ready)
@@ -82,6 +85,9 @@ CASES = [
     (H.Case(shapes=[(300_001,), (77,)], nd=3, clip=0.5, steps=3, weight_decay=0.01), 65536),
     (H.Case(shapes=[(1 << 20,)], nd=8, steps=3), 1 << 20),            # one bucket
     (H.Case(shapes=[(5000,)], nd=4, clip=1.0, steps=2), 64),         # many tiny buckets
+    # static scale with skip_on_overflow: +inf at step 2 and NaN at step 3 both skip
+    (H.Case(shapes=[(200_003,)], nd=8, skip_on_overflow=1, steps=4, inf_steps=(2,),
+            nan_steps=(3,)), 32768),
 ]
 
 

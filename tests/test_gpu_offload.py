@@ -87,6 +87,8 @@ CASES = [
     H.Case(shapes=[(1000,), (24,)], nd=1, steps=2),
     H.Case(shapes=[(5000,)], nd=5, dtype=gen.FP16, grad_sigma=1e-2, loss_scale=1024.0,
            weight_decay=0.01, decoupled_wd=0, steps=2),
+    # static scale with skip_on_overflow: the step with +inf skipped, nothing copied back
+    H.Case(shapes=[(70_001,)], nd=4, skip_on_overflow=1, steps=4, inf_steps=(2,)),
 ]
 
 

@@ -287,6 +287,14 @@ def test_tma_staged_reduce(z, psi, nd, dtype):
     check(z, c, g32=True, reduce_kernel=1)
 
 
+def test_tma_staged_reduce_skip_on_overflow(z):
+    # static bf16 scale with skip_on_overflow through the TMA-staged reduce: the
+    # step with +inf is skipped, the scale kept, the reduced gradient bit-exact
+    c = H.Case(shapes=[(300_000,)], nd=16, skip_on_overflow=1, steps=3, inf_steps=(2,))
+    gpu, _ = check(z, c, g32=True, reduce_kernel=1)
+    assert [r["skipped"] for r in gpu.results] == [0, 1, 0]
+
+
 def test_tma_staged_reduce_rejects_unsupported(z):
     for nd, kw in ((2, dict(clip=1.0)), (8, dict()), (64, dict(clip=1.0))):
         c = H.Case(shapes=[(4096,)], nd=nd, **kw)

@@ -75,6 +75,7 @@ struct zero_plan {
     int64_t launches = 0;
     // bucketed steps (constant-size gradient buckets)
     uint64_t bucket_elems = 0, nbuckets = 0, bucket_ws = 0;
+    int bucket_grid = 0, bucket_last_grid = 0;   // reduce blocks of a full / the last bucket
     std::vector<uint8_t> bucket_seen;
     const void* fn_bucket_reduce = nullptr;
     const void* fn_bucket_final = nullptr;
@@ -576,6 +577,7 @@ zero_status_t zero_plan_set_bucket(zero_plan_t plan, uint64_t bucket_elems,
     if (plan->stepped && cudaEventSynchronize(plan->ev_done) != cudaSuccess) return ZERO_ECUDA;
     if (bucket_elems == 0) {
         plan->bucket_elems = plan->nbuckets = plan->bucket_ws = 0;
+        plan->bucket_grid = plan->bucket_last_grid = 0;
         plan->bucket_seen.clear();
         if (workspace_bytes) *workspace_bytes = 0;
         return ZERO_OK;
@@ -588,10 +590,17 @@ zero_status_t zero_plan_set_bucket(zero_plan_t plan, uint64_t bucket_elems,
     const void* fin = step_kernel((int)plan->dtype, K_BUCKET_FINALIZE, 0);
     const void* upd = step_kernel((int)plan->dtype, K_UPDATE_G32, plan->nd);
     if (!red || !fin || !upd) return ZERO_EINVAL;
+    // each bucket's reduce grid (a full bucket's, and the last bucket's) and its
+    // per-block partial slots
+    const int grid = grid_reduce(red, plan->sms, bucket_elems, REDUCE_WAVES);
+    const int last = grid_reduce(red, plan->sms, plan->n - (nb - 1) * bucket_elems, REDUCE_WAVES);
     plan->bucket_elems = bucket_elems;
     plan->nbuckets = nb;
-    plan->bucket_ws = round_up(plan->n * sizeof(float), 256) + round_up(nb * sizeof(double), 256) +
-                      round_up(nb * sizeof(int32_t), 256);
+    plan->bucket_grid = grid;
+    plan->bucket_last_grid = last;
+    plan->bucket_ws = round_up(plan->n * sizeof(float), 256) +
+                      round_up(nb * (uint64_t)grid * sizeof(double), 256) +
+                      round_up(nb * (uint64_t)grid * sizeof(int32_t), 256);
     try {
         plan->bucket_seen.assign((size_t)nb, 0);
     } catch (...) {
@@ -606,6 +615,8 @@ zero_status_t zero_plan_set_bucket(zero_plan_t plan, uint64_t bucket_elems,
 }
 
 namespace {
+// The bucketed step's workspace: the fp32 reduced gradient [n], then every
+// bucket's per-block squared-norm partials [nb][grid] and overflow flags [nb][grid].
 void bucket_pointers(const zero_plan* plan, void* workspace, float** g32, double** partial,
                      int32_t** flag)
 {
@@ -613,7 +624,7 @@ void bucket_pointers(const zero_plan* plan, void* workspace, float** g32, double
     *g32 = reinterpret_cast<float*>(w);
     w += round_up(plan->n * sizeof(float), 256);
     *partial = reinterpret_cast<double*>(w);
-    w += round_up(plan->nbuckets * sizeof(double), 256);
+    w += round_up(plan->nbuckets * (uint64_t)plan->bucket_grid * sizeof(double), 256);
     *flag = reinterpret_cast<int32_t*>(w);
 }
 }  // namespace
@@ -640,10 +651,10 @@ zero_status_t zero_step_bucket(zero_plan_t plan, uint64_t bucket, const void* bu
     a.n = (int64_t)count;
     a.rank_stride = (int64_t)plan->bucket_elems;
     a.bucket = (int)bucket;
-    a.bucket_partial = partial;
-    a.bucket_flag = flag;
+    a.bucket_partial = partial + bucket * (uint64_t)plan->bucket_grid;
+    a.bucket_flag = flag + bucket * (uint64_t)plan->bucket_grid;
     void* args[] = {&a};
-    const int grid = grid_reduce(plan->fn_bucket_reduce, plan->sms, count, REDUCE_WAVES);
+    const int grid = bucket == plan->nbuckets - 1 ? plan->bucket_last_grid : plan->bucket_grid;
     // A programmatic dependent launch: the blocks may be placed while the previous
     // grid on the stream finishes; the kernel waits (griddepcontrol.wait) for that
     // grid's completion before its first read, so this is safe whatever that grid
@@ -687,10 +698,12 @@ zero_status_t zero_step_apply(zero_plan_t plan, float* master, float* m, float* 
     StepArgs a = step_args(plan, nullptr, master, m, v, params, g32);
     a.bucket_partial = partial;
     a.bucket_flag = flag;
-    int nb = (int)plan->nbuckets;
+    int nb = (int)plan->nbuckets, grid = plan->bucket_grid, last = plan->bucket_last_grid;
+    const unsigned fblocks = (unsigned)std::min<uint64_t>(
+        std::min<uint64_t>(plan->nbuckets, 4ull * (uint64_t)plan->sms), ZERO_MAX_BLOCKS);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    void* fargs[] = {&a, &nb};
-    if (cudaLaunchKernel(plan->fn_bucket_final, dim3(1), dim3(ZERO_THREADS), fargs, 0, s) !=
+    void* fargs[] = {&a, &nb, &grid, &last};
+    if (cudaLaunchKernel(plan->fn_bucket_final, dim3(fblocks), dim3(ZERO_THREADS), fargs, 0, s) !=
         cudaSuccess)
         return ZERO_ECUDA;
     void* uargs[] = {&a};

@@ -77,8 +77,10 @@ struct StepArgs {
     float*    qscales = nullptr;
     // bucketed step: the reduce pass covers one bucket and records its partial
     int       bucket = -1;                // -1: a whole step
-    double*   bucket_partial = nullptr;   // [nbuckets] squared-norm partial of each bucket
-    int32_t*  bucket_flag = nullptr;      // [nbuckets] overflow flag of each bucket
+    // a bucket's reduce: this bucket's per-block squared-norm partials and flags;
+    // the apply step: every bucket's, [nbuckets][bucket_grid]
+    double*   bucket_partial = nullptr;
+    int32_t*  bucket_flag = nullptr;
 };
 
 // ---- 16-bit formats --------------------------------------------------------

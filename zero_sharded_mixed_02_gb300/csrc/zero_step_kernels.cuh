@@ -82,12 +82,21 @@ struct RedShared {
     int    last;
 };
 
-// Publish this block's partial; the last block to arrive finalizes the step.
+// Publish this block's partial; the last block to arrive finalizes the step.  A
+// bucket's reduce only stores its blocks' partials: the apply step combines every
+// bucket's, so a bucket's grid ends with its last block's store.
 static __device__ __forceinline__ void reduce_and_finalize(const StepArgs& a, double acc, int bad,
                                                     RedShared& sh)
 {
     const double bsum = block_sum(acc, sh.d);
     const int    bbad = block_or(bad, sh.i);
+    if (a.bucket >= 0) {
+        if (threadIdx.x == 0) {
+            a.bucket_partial[blockIdx.x] = bsum;
+            a.bucket_flag[blockIdx.x] = bbad;
+        }
+        return;
+    }
     if (threadIdx.x == 0) {
         a.state->partial[blockIdx.x] = bsum;
         a.state->flag[blockIdx.x]    = bbad;
@@ -107,32 +116,37 @@ static __device__ __forceinline__ void reduce_and_finalize(const StepArgs& a, do
     const double total = block_sum(x, sh.d);
     const int    any   = block_or(f, sh.i);
     if (threadIdx.x == 0) {
-        if (a.bucket >= 0) {                       // one bucket of a bucketed step
-            a.bucket_partial[a.bucket] = total;
-            a.bucket_flag[a.bucket] = any;
-        } else {
-            finalize(a, total, any);
-        }
+        finalize(a, total, any);
         a.state->counter = 0;
     }
 }
 
 // Bucketed step, after every bucket is reduced: the global norm and overflow flag
-// from the bucket partials, combined in bucket order by one block, then the
-// step's scalar bookkeeping.
+// from every bucket's per-block partials ([nbuckets][grid], the last bucket using
+// its first last_grid slots), then the step's scalar bookkeeping.  Block f of
+// the grid takes the buckets [nb f / F, nb (f+1) / F) in bucket order, each
+// thread the slots t, t + 256, ... of each; the block sums are combined in block
+// order by the last block to arrive.  The order is fixed by the plan's layout.
 template <int DT>
-__global__ void __launch_bounds__(ZERO_THREADS) k_bucket_finalize(const StepArgs a, int nbuckets)
+__global__ void __launch_bounds__(ZERO_THREADS) k_bucket_finalize(const StepArgs a, int nbuckets,
+                                                                  int grid, int last_grid)
 {
     __shared__ RedShared sh;
+    const int F = gridDim.x;
+    const int b0 = (int)((int64_t)nbuckets * blockIdx.x / F);
+    const int b1 = (int)((int64_t)nbuckets * (blockIdx.x + 1) / F);
     double x = 0.0;
     int f = 0;
-    for (int b = threadIdx.x; b < nbuckets; b += blockDim.x) {
-        x += a.bucket_partial[b];
-        f |= a.bucket_flag[b];
+    for (int b = b0; b < b1; b++) {
+        const int slots = b == nbuckets - 1 ? last_grid : grid;
+        const double* p = a.bucket_partial + (int64_t)b * grid;
+        const int32_t* q = a.bucket_flag + (int64_t)b * grid;
+        for (int s = threadIdx.x; s < slots; s += blockDim.x) {
+            x += p[s];
+            f |= q[s];
+        }
     }
-    const double total = block_sum(x, sh.d);
-    const int any = block_or(f, sh.i);
-    if (threadIdx.x == 0) finalize(a, total, any);
+    reduce_and_finalize(a, x, f, sh);
 }
 
 static __device__ __forceinline__ void unpack8(const float4 a, const float4 b, float (&x)[8])
