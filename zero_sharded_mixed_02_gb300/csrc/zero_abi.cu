@@ -98,6 +98,15 @@ bool finite_f(float x) { return std::isfinite(x); }
 
 zero_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? ZERO_OK : ZERO_ECUDA; }
 
+// 1 - beta^(t+1) from beta^t, as the device's step bookkeeping computes it: one
+// binary64 product, one binary64 difference, one rounding to binary32 (the
+// volatile keeps the host compiler from fusing the two into one rounding).
+float next_bias_correction(double beta_pow, float beta)
+{
+    volatile double prod = beta_pow * (double)beta;
+    return (float)(1.0 - prod);
+}
+
 zero_status_t check_hparams(const zero_hparams_t& h, zero_dtype_t dtype)
 {
     if (!finite_f(h.lr) || !finite_f(h.eps) || h.eps < 0.0f) return ZERO_EINVAL;
@@ -323,6 +332,8 @@ zero_status_t create_impl(uint64_t psi, int nd, int stage, zero_dtype_t dtype,
     init->sc.t = 0;
     init->sc.beta1_pow = 1.0;
     init->sc.beta2_pow = 1.0;
+    init->sc.bc1_next = next_bias_correction(1.0, hp->beta1);
+    init->sc.bc2_next = next_bias_correction(1.0, hp->beta2);
     init->st.clip_coef = 1.0f;
     init->st.used_scale = hp->loss_scale;
     e = cudaMemcpy(p->d_state, init, sizeof(DevState), cudaMemcpyHostToDevice);
@@ -431,6 +442,8 @@ zero_status_t plan_scalars_set(zero_plan_t plan, const PlanScalars& in)
     sc.t = in.t;
     sc.beta1_pow = in.beta1_pow;
     sc.beta2_pow = in.beta2_pow;
+    sc.bc1_next = next_bias_correction(in.beta1_pow, plan->hp.beta1);
+    sc.bc2_next = next_bias_correction(in.beta2_pow, plan->hp.beta2);
     DevStatus st{};
     st.clip_coef = 1.0f;
     st.used_scale = in.loss_scale;

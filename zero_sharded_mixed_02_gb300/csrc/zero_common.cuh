@@ -24,6 +24,11 @@ struct DevScalars {
     int64_t t;
     double  beta1_pow;   // beta1^t by repeated multiplication
     double  beta2_pow;
+    // the next step's bias corrections, 1 - beta^(t+1) rounded to binary32 from
+    // double: kept here by the one thread that advances t, so the fused pass's
+    // threads read them instead of each computing them in binary64
+    float   bc1_next;
+    float   bc2_next;
 };
 
 // What one step reports; written by the last block of the reduce pass.

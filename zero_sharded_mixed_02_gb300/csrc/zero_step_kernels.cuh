@@ -64,6 +64,8 @@ static __device__ __noinline__ void finalize(const StepArgs a, double sumsq, int
         sc.beta2_pow = __dmul_rn(sc.beta2_pow, (double)a.k.b2);
         st.bc1 = __double2float_rn(__dsub_rn(1.0, sc.beta1_pow));
         st.bc2 = __double2float_rn(__dsub_rn(1.0, sc.beta2_pow));
+        sc.bc1_next = __double2float_rn(__dsub_rn(1.0, __dmul_rn(sc.beta1_pow, (double)a.k.b1)));
+        sc.bc2_next = __double2float_rn(__dsub_rn(1.0, __dmul_rn(sc.beta2_pow, (double)a.k.b2)));
         if (a.dynamic && a.growth_interval > 0) {
             sc.good_steps += 1;
             if (sc.good_steps >= a.growth_interval) {
@@ -403,9 +405,8 @@ static __device__ __forceinline__ void fused_pass(const StepArgs& a)
     const int nd = ND > 0 ? ND : a.nd;
     Unscale un;
     un.init(nd, sc.loss_scale);
-    // bias corrections of step t+1 (this path never skips)
-    const float bc1 = __double2float_rn(__dsub_rn(1.0, __dmul_rn(sc.beta1_pow, (double)a.k.b1)));
-    const float bc2 = __double2float_rn(__dsub_rn(1.0, __dmul_rn(sc.beta2_pow, (double)a.k.b2)));
+    // bias corrections of step t+1 (this path never skips), kept by the last step
+    const float bc1 = sc.bc1_next, bc2 = sc.bc2_next;
     double acc = 0.0;
     int bad = 0;
     const int64_t nvec = a.n >> 3;
