@@ -522,8 +522,80 @@ def run_ours(args):
                       f"one full oracle step each ({reps} steps, {per:.3f} s/step)"}
 
     z.zero_plan_destroy(plan)
+
+    # ---- the other workloads, measured in the same run (rank 0, N = 1 only) ----
+    if rank == 0 and ws == 1 and not args.no_other_configs:
+        del grads, master, m, v, params, work
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
+        out["other_configs"] = other_configs(args)
+
     if rank == 0:
         print(json.dumps(out), flush=True)
+
+
+def workload_point(w, k: int) -> dict:
+    """One stages 0-2 workload through zero_step: 3 warm-up steps, then k timed
+    steps on the device (L2 flushed between steps when the inputs would fit in
+    it); step time, params/s and GB/s on the 2Nd + 26 roofline bytes."""
+    import torch
+    import gen
+    import zero_sharded_mixed_02_gb300 as z
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    peak, _ = measured_peaks()
+    plan = _plan_for(z, w)
+    try:
+        _, padded, _, ws = z.zero_plan_layout(plan)
+        grads = torch.empty((w.nd, padded), dtype=torch.int16, device=dev)
+        master = torch.zeros(padded, dtype=torch.float32, device=dev)
+        m, v = torch.zeros_like(master), torch.zeros_like(master)
+        params = torch.zeros(padded, dtype=torch.int16, device=dev)
+        work = torch.empty(max(ws, 16) // 4, dtype=torch.float32, device=dev)
+        gen.cuda_ranks_16(grads.data_ptr(), w.seed, gen.STREAM_GRAD, 1, w.nd, w.psi, w.grad_sigma,
+                          w.loss_scale, w.dtype, rank_stride=padded, cuda_stream=sp)
+        gen.cuda_f32(master.data_ptr(), w.seed, gen.STREAM_MASTER, 0, 0, w.psi, w.master_sigma,
+                     cuda_stream=sp)
+
+        def step():
+            z.zero_step(plan, grads, master, m, v, params, work, sp)
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize(dev)
+        small = (2 * w.nd + 14) * padded <= (1 << 30)
+        ms = _timed_steps(torch, stream, step, k, l2_flush(torch, dev) if small else None) / k
+        roof = (2 * w.nd + 26) * w.psi
+        return {"psi": w.psi, "nd": w.nd, "stage": w.stage, "path": z.zero_plan_path(plan),
+                "ms_per_step": ms, "params_per_s": w.psi / (ms / 1e3),
+                "hbm_gbs_roofline_bytes": roof / (ms / 1e3) / 1e9,
+                "frac_of_measured_hbm": roof / (ms / 1e3) / 1e9 / peak, "steps": k,
+                "l2": "flushed between steps" if small else "inputs larger than L2"}
+    finally:
+        z.zero_plan_destroy(plan)
+        torch.cuda.empty_cache()
+
+
+def other_configs(args) -> dict:
+    """The other workloads of the benchmark's configuration list, each timed on the
+    device in this run: the tiny flat model, GPT-2 small, LLaMA-3-8B ZeRO-3 (the
+    resident shard's update, the 34 unit gathers, and the 4-bit qwZ step), and two
+    points of the bandwidth sweep.  A workload that fails is recorded, not fatal."""
+    import argparse
+    from gen import workloads as W
+    res = {}
+    jobs = [("tiny-flat-4t", lambda: workload_point(W.tiny(), 200)),
+            ("gpt2-small", lambda: workload_point(W.gpt2_small(), 20)),
+            ("llama3-8b", lambda: stage3_measure(argparse.Namespace(
+                layers=0, vocab=0, nd=0, qwz=4, warmup=3, steps=10))),
+            ("sweep-2^24-nd8", lambda: workload_point(W.sweep(1 << 24, 8), 200)),
+            ("sweep-2^28-nd8", lambda: workload_point(W.sweep(1 << 28, 8), 20))]
+    for name, fn in jobs:
+        try:
+            res[name] = fn()
+        except Exception as e:                      # noqa: BLE001 -- recorded in the line
+            res[name] = {"error": f"{type(e).__name__}: {e}"}
+    return res
 
 
 def e2e_leg(args, z, plan, w, grads, master, m, v, params, work, dev, stream):
@@ -725,6 +797,11 @@ def run_stage3(args):
     """LLaMA-3-8B at Nd = 64, ZeRO-3: one step = the update of rank 0's resident
     shard from its 64 contributions, then the gather of every unit (34) from the
     64 ranks' parameter shards into one buffer."""
+    print(json.dumps(stage3_measure(args)), flush=True)
+
+
+def stage3_measure(args) -> dict:
+    """The measurements run_stage3 prints, as a dict (buffers freed on return)."""
     import torch
     import gen
     import zero_sharded_mixed_02_gb300 as z
@@ -831,7 +908,7 @@ def run_stage3(args):
                    "vs_unquantized_step": (t_upd + t_gat) / t_sq,
                    "vs_separate_update_quantize_gather": (t_upd + t_q) / t_sq}}
     desc = DESCRIPTIONS.get(w.name, f"LLaMA-3-8B-shaped list scaled to {len(units) - 2} layers")
-    print(json.dumps({
+    res = {
         "mode": "zero3", "metric": "ZeRO-3 step: resident-shard update and per-unit gathers",
         "workload": f"{w.name}: {desc}, {len(w.shapes)} tensors, {nunits} units",
         "psi": w.psi, "nd": w.nd, "shard_elems": total, "steps": K,
@@ -843,8 +920,9 @@ def run_stage3(args):
                                  "gather": gat_bytes / (t_gat / 1e3) / 1e9 / peak},
         "qwz": qwz or None,
         "l2": (f"inputs larger than L2 ({2 * w.nd * total / 1e9:.1f} GB gradients, "
-               f"{2 * (w.nd - 1) * total / 1e9:.1f} GB shards)")}), flush=True)
+               f"{2 * (w.nd - 1) * total / 1e9:.1f} GB shards)")}
     z.zero_plan_destroy(plan)
+    return res
 
 
 def run_buckets(args):
@@ -1180,6 +1258,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="skip the other workloads measured after the headline")
     ap.add_argument("--cpu-sample", type=int, default=1 << 23)
     ap.add_argument("--ref-sample", type=int, default=1 << 21)
     ap.add_argument("--reduce-kernel", choices=("ldg", "tma"), default="ldg",
