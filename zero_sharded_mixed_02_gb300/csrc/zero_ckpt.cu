@@ -83,7 +83,7 @@ uint64_t zck64(const void* data, uint64_t bytes, uint64_t w0)
         h2 += mix64(x[2] + k + 2 * GOLDEN);
         h3 += mix64(x[3] + k + 3 * GOLDEN);
     }
-    for (; i < words; i++) {
+    for (unsigned j = 0; j < (unsigned)(words & 3); j++, i++) {   // the last 0-3 words
         uint64_t x;
         std::memcpy(&x, p + 8 * i, 8);
         h0 += mix64(x + (w0 + i + 1) * GOLDEN);
