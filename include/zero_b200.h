@@ -298,6 +298,31 @@ zero_status_t zero_step_qwz(zero_plan_t plan, const void* grads, float* master, 
                             void* params, void* workspace, int bits, void* codes, float* scales,
                             void* stream);
 
+/* ---- ping-pong step ------------------------------------------------------- */
+
+/* One optimizer step as a single pass over the data even when an overflow may
+ * skip it (dynamic loss scaling or skip_on_overflow, without a clip): the
+ * caller keeps two sets of master, m, v; the step reads the current set and
+ * writes the other, and only a step that is not skipped makes the other set
+ * current, so a skipped step leaves the current state untouched without having
+ * to know the overflow before the update.  The 16-bit parameters are written by
+ * the pass; when the step is skipped, a small pass after it rewrites them from
+ * the current set's master (4 + 2 bytes per element, on skipped steps only).
+ * The arithmetic is zero_step's: the same state, parameters and report.
+ *   set 0: master0, m0, v0; set 1: master1, m1, v1; each laid out as zero_step's
+ *          master, m, v (stages 0-2: [nd*S]; stage 3: the resident shard).
+ *   grads, params: as zero_step.
+ * zero_plan_state_set reports which set is current after the plan's last step
+ * (waiting for it): 0 after zero_plan_create and after zero_checkpoint_load
+ * (load a checkpoint into set 0); checkpoint the current set.  A plan may mix
+ * zero_step and zero_step_pingpong only if the caller passes the current set
+ * to zero_step.  Asynchronous.  Errors: ZERO_EINVAL (clip_norm > 0, null or
+ * misaligned pointer), ZERO_ESTATE, ZERO_ECUDA. */
+zero_status_t zero_step_pingpong(zero_plan_t plan, const void* grads, float* master0, float* m0,
+                                 float* v0, float* master1, float* m1, float* v1, void* params,
+                                 void* stream);
+zero_status_t zero_plan_state_set(zero_plan_t plan, int* set);
+
 /* ---- gradient norm without allocating ------------------------------------ */
 
 /* No counterpart on the pages: a convenience for callers that may not

@@ -31,7 +31,8 @@ PATH_FUSED, PATH_G32, PATH_RECOMPUTE = 0, 1, 2
 # every entry point declared in include/zero_b200.h
 ENTRY_POINTS = (
     "zero_plan_create", "zero_plan_create_units", "zero_plan_destroy", "zero_plan_layout",
-    "zero_plan_unit", "zero_step", "zero_step_qwz", "zero_step_result", "zero_step_overflow",
+    "zero_plan_unit", "zero_step", "zero_step_qwz", "zero_step_pingpong", "zero_plan_state_set",
+    "zero_step_result", "zero_step_overflow",
     "zero_gather_layer", "zero_state_bytes", "zero_comm_volume", "zero_max_params",
     "zero_status_string", "zero_plan_profile", "zero_plan_kernel_times", "zero_plan_path",
     "zero_grad_norm_noalloc", "zero_plan_set_reduce_kernel", "zero_quantize_shard",
@@ -89,6 +90,8 @@ def lib():
                 "zero_plan_unit": (st, [_P, ctypes.c_int, _PU64, _PU64, _PU64]),
                 "zero_step": (st, [_P, _P, _P, _P, _P, _P, _P, _P]),
                 "zero_step_qwz": (st, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_int, _P, _P, _P]),
+                "zero_step_pingpong": (st, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+                "zero_plan_state_set": (st, [_P, ctypes.POINTER(ctypes.c_int)]),
                 "zero_step_result": (st, [_P, ctypes.POINTER(ctypes.c_int),
                                           ctypes.POINTER(ctypes.c_double),
                                           ctypes.POINTER(ctypes.c_float),
@@ -226,6 +229,20 @@ def zero_step_qwz(plan: int, grads, master, m, v, params, workspace, bits: int, 
     _check(lib().zero_step_qwz(plan, _ptr(grads), _ptr(master), _ptr(m), _ptr(v), _ptr(params),
                                _ptr(workspace), bits, _ptr(codes), _ptr(scales), _ptr(stream)),
            "zero_step_qwz")
+
+
+def zero_step_pingpong(plan: int, grads, set0, set1, params, stream=0) -> None:
+    """set0, set1: (master, m, v) each."""
+    (p0, m0, v0), (p1, m1, v1) = set0, set1
+    _check(lib().zero_step_pingpong(plan, _ptr(grads), _ptr(p0), _ptr(m0), _ptr(v0), _ptr(p1),
+                                    _ptr(m1), _ptr(v1), _ptr(params), _ptr(stream)),
+           "zero_step_pingpong")
+
+
+def zero_plan_state_set(plan: int) -> int:
+    s = ctypes.c_int()
+    _check(lib().zero_plan_state_set(plan, ctypes.byref(s)), "zero_plan_state_set")
+    return s.value
 
 
 def zero_step_result(plan: int) -> dict:

@@ -59,6 +59,10 @@ struct zero_plan {
     // on first use: the single pass, or the update pass of the two-pass paths
     const void* fn_q[2] = {nullptr, nullptr};
     int grid_q[2] = {1, 1};
+    // ping-pong steps, resolved on first use: the single pass and its repair pass
+    const void* fn_pp = nullptr;
+    const void* fn_pp_repair = nullptr;
+    int grid_pp = 1;
     // device
     int device = 0, sms = 1;
     DevState* d_state = nullptr;
@@ -444,6 +448,7 @@ zero_status_t plan_scalars_set(zero_plan_t plan, const PlanScalars& in)
     sc.beta2_pow = in.beta2_pow;
     sc.bc1_next = next_bias_correction(in.beta1_pow, plan->hp.beta1);
     sc.bc2_next = next_bias_correction(in.beta2_pow, plan->hp.beta2);
+    sc.cur = 0;                         // a restored state is the ping-pong set 0
     DevStatus st{};
     st.clip_coef = 1.0f;
     st.used_scale = in.loss_scale;
@@ -774,7 +779,7 @@ namespace {
 
 // Validation shared by zero_step and zero_step_qwz.
 zero_status_t check_step_args(const zero_plan* plan, const void* grads, float* master, float* m,
-                              float* v, void* params, void* workspace)
+                              float* v, void* params, void* workspace, bool uses_workspace = true)
 {
     if (plan->poisoned) return ZERO_ESTATE;
     if (plan->n > 0) {
@@ -782,7 +787,8 @@ zero_status_t check_step_args(const zero_plan* plan, const void* grads, float* m
         for (const void* q : ptrs)
             if (!q || !aligned16(q)) return ZERO_EINVAL;
     }
-    if (plan->path == PATH_G32 && plan->n > 0 && (!workspace || !aligned16(workspace)))
+    if (uses_workspace && plan->path == PATH_G32 && plan->n > 0 &&
+        (!workspace || !aligned16(workspace)))
         return ZERO_EINVAL;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return ZERO_ECUDA;
@@ -791,11 +797,11 @@ zero_status_t check_step_args(const zero_plan* plan, const void* grads, float* m
 }
 
 // The step's launch sequence: pass 1 (fn_a; the fused pass, or the reduce pass
-// in the plan's configured form), then, on the two-pass paths, pass 2 (fn_b) as
-// its programmatic dependent; per-kernel events when profiling; the step's
-// completion event.
+// in the plan's configured form), then, when fn_b is given, pass 2 (fn_b, grid_b
+// blocks) as its programmatic dependent; per-kernel events when profiling; the
+// step's completion event.
 zero_status_t launch_step(zero_plan* plan, StepArgs& a, const void* fn_a, int grid_a,
-                          const void* fn_b, cudaStream_t s)
+                          const void* fn_b, uint64_t grid_b, cudaStream_t s)
 {
     ProfileSlot* slot = nullptr;
     if (plan->profile) {
@@ -820,7 +826,7 @@ zero_status_t launch_step(zero_plan* plan, StepArgs& a, const void* fn_a, int gr
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)plan->grid_b);
+        cfg.gridDim = dim3((unsigned)grid_b);
         cfg.blockDim = dim3(ZERO_THREADS);
         cfg.dynamicSmemBytes = 0;
         cfg.stream = s;
@@ -852,7 +858,7 @@ zero_status_t zero_step(zero_plan_t plan, const void* grads, float* master, floa
     const zero_status_t st = check_step_args(plan, grads, master, m, v, params, workspace);
     if (st != ZERO_OK) return st;
     StepArgs a = step_args(plan, grads, master, m, v, params, workspace);
-    return launch_step(plan, a, plan->fn_a, plan->grid_a, plan->fn_b,
+    return launch_step(plan, a, plan->fn_a, plan->grid_a, plan->fn_b, plan->grid_b,
                        static_cast<cudaStream_t>(stream));
 }
 
@@ -883,9 +889,49 @@ zero_status_t zero_step_qwz(zero_plan_t plan, const void* grads, float* master, 
     a.qcodes = static_cast<uint8_t*>(codes);
     a.qscales = scales;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (plan->path == PATH_FUSED) return launch_step(plan, a, plan->fn_q[q], plan->grid_q[q],
-                                                     nullptr, s);
-    return launch_step(plan, a, plan->fn_a, plan->grid_a, plan->fn_q[q], s);
+    if (plan->path == PATH_FUSED)
+        return launch_step(plan, a, plan->fn_q[q], plan->grid_q[q], nullptr, 0, s);
+    return launch_step(plan, a, plan->fn_a, plan->grid_a, plan->fn_q[q], plan->grid_b, s);
+}
+
+zero_status_t zero_step_pingpong(zero_plan_t plan, const void* grads, float* master0, float* m0,
+                                 float* v0, float* master1, float* m1, float* v1, void* params,
+                                 void* stream)
+{
+    zero::TraceRange trace_("zero_step_pingpong");
+    if (!plan || plan->hp.clip_norm > 0.0f) return ZERO_EINVAL;   // a clip gates the update
+    const zero_status_t st = check_step_args(plan, grads, master0, m0, v0, params, nullptr, false);
+    if (st != ZERO_OK) return st;
+    if (plan->n > 0) {
+        const void* ptrs[] = {master1, m1, v1};
+        for (const void* q : ptrs)
+            if (!q || !aligned16(q)) return ZERO_EINVAL;
+    }
+    if (!plan->fn_pp) {
+        const void* fn = step_kernel((int)plan->dtype, K_FUSED_PP, plan->nd);
+        const void* rep = step_kernel((int)plan->dtype, K_PP_REPAIR, 0);
+        if (!fn || !rep) return ZERO_EINVAL;
+        plan->grid_pp = grid_reduce(fn, plan->sms, plan->n, FUSED_WAVES);
+        plan->fn_pp = fn;
+        plan->fn_pp_repair = rep;
+    }
+    StepArgs a = step_args(plan, grads, master0, m0, v0, params, nullptr);
+    a.master2 = master1;
+    a.m2 = m1;
+    a.v2 = v1;
+    a.pingpong = 1;
+    // the repair pass: one thread per 4 elements, like the update pass
+    return launch_step(plan, a, plan->fn_pp, plan->grid_pp, plan->fn_pp_repair, plan->grid_b,
+                       static_cast<cudaStream_t>(stream));
+}
+
+zero_status_t zero_plan_state_set(zero_plan_t plan, int* set)
+{
+    if (!plan || !set) return ZERO_EINVAL;
+    const zero_status_t s = fetch_mirror(plan);
+    if (s != ZERO_OK) return s;
+    *set = plan->h_mirror->cur;
+    return ZERO_OK;
 }
 
 zero_status_t zero_step_result(zero_plan_t plan, int* skipped, double* grad_norm,

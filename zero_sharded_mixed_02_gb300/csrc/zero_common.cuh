@@ -29,6 +29,10 @@ struct DevScalars {
     // threads read them instead of each computing them in binary64
     float   bc1_next;
     float   bc2_next;
+    // ping-pong steps: which of the caller's two state sets holds the current
+    // master, m, v (0 after plan creation and after a checkpoint load)
+    int32_t cur;
+    int32_t pad;
 };
 
 // What one step reports; written by the last block of the reduce pass.
@@ -76,6 +80,12 @@ struct StepArgs {
     float     backoff;
     int       growth_interval;
     DevState* state;
+    // ping-pong step: the second set of master, m, v; the step reads set `cur`
+    // (DevScalars) and writes the other, and a step that is not skipped flips cur
+    float*    master2 = nullptr;
+    float*    m2 = nullptr;
+    float*    v2 = nullptr;
+    int       pingpong = 0;
     // ZeRO-3 step with the qwZ quantizer in its epilogue: the updated 16-bit
     // parameters' block codes and scales (as zero_quantize_shard writes them)
     uint8_t*  qcodes = nullptr;

@@ -21,7 +21,10 @@ enum Kind {
     K_UPDATE_G32_Q8 = 9,
     K_UPDATE_G32_Q4 = 10,
     K_UPDATE_RECOMPUTE_Q8 = 11,
-    K_UPDATE_RECOMPUTE_Q4 = 12
+    K_UPDATE_RECOMPUTE_Q4 = 12,
+    // ping-pong steps (zero_step_pingpong): the single pass and its repair pass
+    K_FUSED_PP = 13,
+    K_PP_REPAIR = 14
 };
 
 // Kernel function for (dtype, kind, nd); nullptr if that combination is not

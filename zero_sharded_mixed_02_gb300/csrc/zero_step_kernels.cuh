@@ -66,6 +66,7 @@ static __device__ __noinline__ void finalize(const StepArgs a, double sumsq, int
         st.bc2 = __double2float_rn(__dsub_rn(1.0, sc.beta2_pow));
         sc.bc1_next = __double2float_rn(__dsub_rn(1.0, __dmul_rn(sc.beta1_pow, (double)a.k.b1)));
         sc.bc2_next = __double2float_rn(__dsub_rn(1.0, __dmul_rn(sc.beta2_pow, (double)a.k.b2)));
+        if (a.pingpong) sc.cur ^= 1;           // the step's writes become the state
         if (a.dynamic && a.growth_interval > 0) {
             sc.good_steps += 1;
             if (sc.good_steps >= a.growth_interval) {
@@ -355,15 +356,30 @@ __global__ void __launch_bounds__(ZERO_THREADS) k_update(const StepArgs a)
 // ---- fused single pass (no clip, no dynamic scale, no skip on overflow):
 // stages 1-6a ----------------------------------------------------------------
 // One 8-element vector of the step: fold, unscale, flag, squares, Adam, cast,
-// write-back; returns the 8 new 16-bit parameters packed in w.
-template <int DT, int ND>
+// write-back; returns the 8 new 16-bit parameters packed in w.  PP: a ping-pong
+// step, reading state set `cur` and writing the other one.
+template <int DT, int ND, bool PP = false>
 static __device__ __forceinline__ void fused8(const StepArgs& a, int64_t vi, int nd,
                                               const Unscale& un, float bc1, float bc2,
-                                              double& acc, int& bad, uint4& w)
+                                              double& acc, int& bad, uint4& w, int cur = 0)
 {
     float4* pm = reinterpret_cast<float4*>(a.master);
     float4* mm = reinterpret_cast<float4*>(a.m);
     float4* vv = reinterpret_cast<float4*>(a.v);
+    float4* po = pm;
+    float4* mo = mm;
+    float4* vo = vv;
+    if constexpr (PP) {
+        float4* p2 = reinterpret_cast<float4*>(a.master2);
+        float4* m2 = reinterpret_cast<float4*>(a.m2);
+        float4* v2 = reinterpret_cast<float4*>(a.v2);
+        if (cur) {
+            po = pm; mo = mm; vo = vv;
+            pm = p2; mm = m2; vv = v2;
+        } else {
+            po = p2; mo = m2; vo = v2;
+        }
+    }
     float s[8], g[8], p[8], m[8], v[8];
     const float4 p0 = __ldcs(pm + 2 * vi), p1 = __ldcs(pm + 2 * vi + 1);
     const float4 m0 = __ldcs(mm + 2 * vi), m1 = __ldcs(mm + 2 * vi + 1);
@@ -380,12 +396,12 @@ static __device__ __forceinline__ void fused8(const StepArgs& a, int64_t vi, int
     unpack8(v0, v1, v);
 #pragma unroll
     for (int e = 0; e < 8; e++) adam1(g[e], 1.0f, p[e], m[e], v[e], bc1, bc2, a.k);
-    __stcs(pm + 2 * vi, make_float4(p[0], p[1], p[2], p[3]));
-    __stcs(pm + 2 * vi + 1, make_float4(p[4], p[5], p[6], p[7]));
-    __stcs(mm + 2 * vi, make_float4(m[0], m[1], m[2], m[3]));
-    __stcs(mm + 2 * vi + 1, make_float4(m[4], m[5], m[6], m[7]));
-    __stcs(vv + 2 * vi, make_float4(v[0], v[1], v[2], v[3]));
-    __stcs(vv + 2 * vi + 1, make_float4(v[4], v[5], v[6], v[7]));
+    __stcs(po + 2 * vi, make_float4(p[0], p[1], p[2], p[3]));
+    __stcs(po + 2 * vi + 1, make_float4(p[4], p[5], p[6], p[7]));
+    __stcs(mo + 2 * vi, make_float4(m[0], m[1], m[2], m[3]));
+    __stcs(mo + 2 * vi + 1, make_float4(m[4], m[5], m[6], m[7]));
+    __stcs(vo + 2 * vi, make_float4(v[0], v[1], v[2], v[3]));
+    __stcs(vo + 2 * vi + 1, make_float4(v[4], v[5], v[6], v[7]));
     w = make_uint4(narrow2<DT>(p[0], p[1]), narrow2<DT>(p[2], p[3]), narrow2<DT>(p[4], p[5]),
                    narrow2<DT>(p[6], p[7]));
     __stcs(reinterpret_cast<uint4*>(a.params) + vi, w);
@@ -396,11 +412,13 @@ static __device__ __forceinline__ void fused8(const StepArgs& a, int64_t vi, int
 // starting on a multiple of 256, one quantization block, so the block's absmax
 // is one warp shuffle reduction.  The loop then runs while the warp's first
 // vector is in range, with the lanes past the end idle, so every lane takes the
-// shuffles.
-template <int DT, int ND, int QB>
+// shuffles.  PP: the ping-pong step (state set sc.cur in, the other out), whose
+// repair pass is a programmatic dependent of this grid.
+template <int DT, int ND, int QB, bool PP = false>
 static __device__ __forceinline__ void fused_pass(const StepArgs& a)
 {
     __shared__ RedShared sh;
+    if constexpr (PP) asm volatile("griddepcontrol.launch_dependents;");
     const DevScalars sc = a.state->sc;
     const int nd = ND > 0 ? ND : a.nd;
     Unscale un;
@@ -414,7 +432,7 @@ static __device__ __forceinline__ void fused_pass(const StepArgs& a)
     if constexpr (QB == 0) {
         for (int64_t vi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; vi < nvec; vi += stride) {
             uint4 w;
-            fused8<DT, ND>(a, vi, nd, un, bc1, bc2, acc, bad, w);
+            fused8<DT, ND, PP>(a, vi, nd, un, bc1, bc2, acc, bad, w, PP ? sc.cur : 0);
         }
     } else {
         const int lane = threadIdx.x & 31;
@@ -439,11 +457,24 @@ static __device__ __forceinline__ void fused_pass(const StepArgs& a)
             const float g = un(fold1<DT>(a.grads, a.rank_stride, i, nd));
             bad |= not_finite(g);
             acc = __fma_rn((double)g, (double)g, acc);
-            float p = a.master[i], m = a.m[i], v = a.v[i];
+            float* pi = a.master;
+            float* mi = a.m;
+            float* vi1 = a.v;
+            float* po = pi;
+            float* mo = mi;
+            float* vo = vi1;
+            if constexpr (PP) {
+                if (sc.cur) {
+                    pi = a.master2; mi = a.m2; vi1 = a.v2;
+                } else {
+                    po = a.master2; mo = a.m2; vo = a.v2;
+                }
+            }
+            float p = pi[i], m = mi[i], v = vi1[i];
             adam1(g, 1.0f, p, m, v, bc1, bc2, a.k);
-            a.master[i] = p;
-            a.m[i] = m;
-            a.v[i] = v;
+            po[i] = p;
+            mo[i] = m;
+            vo[i] = v;
             a.params[i] = narrow1<DT>(p);
         }
     }
@@ -454,6 +485,37 @@ template <int DT, int ND>
 __global__ void __launch_bounds__(ZERO_THREADS) k_fused(const StepArgs a)
 {
     fused_pass<DT, ND, 0>(a);
+}
+
+// The ping-pong step's single pass (zero_step_pingpong), held to 3 blocks per SM
+// (2 for the generic rank count): unbounded, the two pointer sets took it to 172
+// registers at nd 64.
+template <int DT, int ND>
+__global__ void __launch_bounds__(ZERO_THREADS, ND == 0 ? 2 : 3) k_fused_pp(const StepArgs a)
+{
+    fused_pass<DT, ND, 0, true>(a);
+}
+
+// After a ping-pong step: when the step was skipped, its pass has already
+// written the 16-bit parameters from the discarded new state, so they are
+// rewritten from the current set's master (cur, unchanged by a skipped step);
+// otherwise nothing.  A programmatic dependent of the pass: it waits for the
+// pass's completion before reading the step status.  One thread per 4 elements.
+template <int DT>
+__global__ void __launch_bounds__(ZERO_THREADS) k_pp_repair(const StepArgs a)
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (!a.state->st.skipped) return;
+    const float* master = a.state->sc.cur ? a.master2 : a.master;
+    const int64_t vi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t nvec = a.n >> 2;
+    if (vi < nvec) {
+        const float4 p = __ldcs(reinterpret_cast<const float4*>(master) + vi);
+        __stcs(reinterpret_cast<uint2*>(a.params) + vi,
+               make_uint2(narrow2<DT>(p.x, p.y), narrow2<DT>(p.z, p.w)));
+    } else if (vi == nvec) {
+        for (int64_t i = nvec << 2; i < a.n; i++) a.params[i] = narrow1<DT>(master[i]);
+    }
 }
 
 // The qwZ instances are held to 4 blocks per SM (64 registers; 2 for the

@@ -30,7 +30,8 @@ static const void* fused_or_reduce(int kind)
 }
 
 // The qwZ-epilogue instances (ZeRO-3 steps that also quantize the updated
-// shard), compiled in their own translation units.
+// shard) and the ping-pong step's passes, compiled in their own translation
+// units.
 template <int DT, int ND>
 static const void* fused_or_update_q(int kind)
 {
@@ -45,6 +46,7 @@ static const void* fused_or_update_q(int kind)
     case K_UPDATE_RECOMPUTE_Q4:
         if constexpr (ND == 0 || ND < 4) return (const void*)k_update<DT, ND, true, 4>;
         return nullptr;
+    case K_FUSED_PP: return (const void*)k_fused_pp<DT, ND>;
     default: return nullptr;
     }
 }
@@ -52,6 +54,7 @@ static const void* fused_or_update_q(int kind)
 template <int DT>
 static const void* step_kernel_q_dt(int kind, int nd)
 {
+    if (kind == K_PP_REPAIR) return (const void*)k_pp_repair<DT>;
     switch (nd) {
     case 1:  return fused_or_update_q<DT, 1>(kind);
     case 2:  return fused_or_update_q<DT, 2>(kind);
