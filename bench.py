@@ -534,10 +534,11 @@ def run_ours(args):
         print(json.dumps(out), flush=True)
 
 
-def workload_point(w, k: int) -> dict:
+def workload_point(w, k: int, pingpong: bool = False) -> dict:
     """One stages 0-2 workload through zero_step: 3 warm-up steps, then k timed
     steps on the device (L2 flushed between steps when the inputs would fit in
-    it); step time, params/s and GB/s on the 2Nd + 26 roofline bytes."""
+    it); step time, params/s and GB/s on the 2Nd + 26 roofline bytes.  pingpong:
+    the same steps through zero_step_pingpong too (two state sets, one pass)."""
     import torch
     import gen
     import zero_sharded_mixed_02_gb300 as z
@@ -564,13 +565,30 @@ def workload_point(w, k: int) -> dict:
             step()
         torch.cuda.synchronize(dev)
         small = (2 * w.nd + 14) * padded <= (1 << 30)
-        ms = _timed_steps(torch, stream, step, k, l2_flush(torch, dev) if small else None) / k
+        flush = l2_flush(torch, dev) if small else None
+        ms = _timed_steps(torch, stream, step, k, flush) / k
         roof = (2 * w.nd + 26) * w.psi
-        return {"psi": w.psi, "nd": w.nd, "stage": w.stage, "path": z.zero_plan_path(plan),
-                "ms_per_step": ms, "params_per_s": w.psi / (ms / 1e3),
-                "hbm_gbs_roofline_bytes": roof / (ms / 1e3) / 1e9,
-                "frac_of_measured_hbm": roof / (ms / 1e3) / 1e9 / peak, "steps": k,
-                "l2": "flushed between steps" if small else "inputs larger than L2"}
+        res = {"psi": w.psi, "nd": w.nd, "stage": w.stage, "path": z.zero_plan_path(plan),
+               "ms_per_step": ms, "params_per_s": w.psi / (ms / 1e3),
+               "hbm_gbs_roofline_bytes": roof / (ms / 1e3) / 1e9,
+               "frac_of_measured_hbm": roof / (ms / 1e3) / 1e9 / peak, "steps": k,
+               "l2": "flushed between steps" if small else "inputs larger than L2"}
+        if pingpong:
+            other = [torch.zeros_like(master) for _ in range(3)]
+
+            def step_pp():
+                z.zero_step_pingpong(plan, grads, (master, m, v), other, params, sp)
+            for _ in range(3):
+                step_pp()
+            torch.cuda.synchronize(dev)
+            ms_pp = _timed_steps(torch, stream, step_pp, k, flush) / k
+            res["pingpong"] = {
+                "what": "zero_step_pingpong: one pass over two state sets, a skipped step "
+                        "rewrites the 16-bit parameters from the current set",
+                "ms_per_step": ms_pp, "params_per_s": w.psi / (ms_pp / 1e3),
+                "frac_of_measured_hbm": roof / (ms_pp / 1e3) / 1e9 / peak,
+                "vs_zero_step": ms / ms_pp}
+        return res
     finally:
         z.zero_plan_destroy(plan)
         torch.cuda.empty_cache()
@@ -584,7 +602,7 @@ def other_configs(args) -> dict:
     import argparse
     from gen import workloads as W
     res = {}
-    jobs = [("tiny-flat-4t", lambda: workload_point(W.tiny(), 200)),
+    jobs = [("tiny-flat-4t", lambda: workload_point(W.tiny(), 200, pingpong=True)),
             ("gpt2-small", lambda: workload_point(W.gpt2_small(), 20)),
             ("llama3-8b", lambda: stage3_measure(argparse.Namespace(
                 layers=0, vocab=0, nd=0, qwz=4, warmup=3, steps=10))),
