@@ -594,6 +594,62 @@ def workload_point(w, k: int, pingpong: bool = False) -> dict:
         torch.cuda.empty_cache()
 
 
+def run_pingpong(args):
+    """The named workload with its clip turned off (fp16 dynamic loss scaling
+    keeps the skip): zero_step (two passes through an fp32 gradient, since the
+    overflow flag must be known before any update) against zero_step_pingpong
+    (one pass over two state sets), K device-timed steps each."""
+    import torch
+    import gen
+    import zero_sharded_mixed_02_gb300 as z
+    from zero_sharded_mixed_02_gb300 import build as zbuild
+    zbuild.build()
+    w = dataclasses.replace(workload(args.psi, args.workload, args.nd), clip=0.0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    peak, _ = measured_peaks()
+    plan = _plan_for(z, w)
+    try:
+        _, padded, _, ws = z.zero_plan_layout(plan)
+        grads = torch.empty((w.nd, padded), dtype=torch.int16, device=dev)
+        sets = [[torch.zeros(padded, dtype=torch.float32, device=dev) for _ in range(3)]
+                for _ in range(2)]
+        params = torch.zeros(padded, dtype=torch.int16, device=dev)
+        work = torch.empty(max(ws, 16) // 4, dtype=torch.float32, device=dev)
+        gen.cuda_ranks_16(grads.data_ptr(), w.seed, gen.STREAM_GRAD, 1, w.nd, w.psi, w.grad_sigma,
+                          w.loss_scale, w.dtype, rank_stride=padded, cuda_stream=sp)
+        gen.cuda_f32(sets[0][0].data_ptr(), w.seed, gen.STREAM_MASTER, 0, 0, w.psi,
+                     w.master_sigma, cuda_stream=sp)
+        K = args.steps
+        small = (2 * w.nd + 14) * padded <= (1 << 30)
+        flush = l2_flush(torch, dev) if small else None
+
+        def two_pass():
+            z.zero_step(plan, grads, *sets[0], params, work, sp)
+
+        def one_pass():
+            z.zero_step_pingpong(plan, grads, sets[0], sets[1], params, sp)
+        for _ in range(max(3, args.warmup)):
+            two_pass()
+        ms2 = _timed_steps(torch, stream, two_pass, K, flush) / K
+        for _ in range(max(3, args.warmup)):
+            one_pass()
+        ms1 = _timed_steps(torch, stream, one_pass, K, flush) / K
+        roof = (2 * w.nd + 26) * w.psi
+        print(json.dumps({
+            "mode": "pingpong", "workload": f"{w.name} with the clip off", "psi": w.psi,
+            "nd": w.nd, "grads": "fp16 dynamic loss scale" if w.dynamic_scale else "static",
+            "zero_step_ms": ms2, "zero_step_pingpong_ms": ms1, "speedup": ms2 / ms1,
+            "roofline_bytes_per_elem": 2 * w.nd + 26,
+            "frac_of_measured_hbm": {"zero_step": roof / (ms2 / 1e3) / 1e9 / peak,
+                                     "zero_step_pingpong": roof / (ms1 / 1e3) / 1e9 / peak},
+            "steps": K, "t": z.zero_step_result(plan)["t"],
+            "state_set": z.zero_plan_state_set(plan)}), flush=True)
+    finally:
+        z.zero_plan_destroy(plan)
+
+
 def other_configs(args) -> dict:
     """The other workloads of the benchmark's configuration list, each timed on the
     device in this run: the tiny flat model, GPT-2 small, LLaMA-3-8B ZeRO-3 (the
@@ -1285,6 +1341,8 @@ def main(argv=None):
     ap.add_argument("--workload", choices=WORKLOADS, default="gpt2-1.5b")
     ap.add_argument("--sweep", action="store_true",
                     help="bandwidth sweep: one JSON line per (psi, nd) point")
+    ap.add_argument("--pingpong", action="store_true",
+                    help="the workload with its clip off: zero_step against zero_step_pingpong")
     ap.add_argument("--offload", action="store_true",
                     help="time ZeRO-Offload steps (device reduce, host Adam) on the workload")
     ap.add_argument("--host-threads", type=int, default=0, help="host threads for --offload")
@@ -1317,6 +1375,8 @@ def main(argv=None):
         run_checkpoint(args)
     elif args.offload:
         run_offload(args)
+    elif args.pingpong:
+        run_pingpong(args)
     elif args.workload == "llama3-8b":
         run_stage3(args)
     else:
