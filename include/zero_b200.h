@@ -341,11 +341,9 @@ zero_status_t zero_plan_state_set(zero_plan_t plan, int* set);
  * 2^17-element tile plus a counter, 196,864 bytes) is a fixed device array in
  * the library that every GPU loading the library keeps until process exit;
  * hence n is limited to 2^31 elements (ZERO_EINVAL beyond).  The first call on
- * a device looks up that array's device address (cudaGetSymbolAddress); make
- * the first call on each device before any stream capture.  The address is
- * kept per device context: after the device's primary context is reset
- * (cudaDeviceReset), the next call looks it up again, so that call too should
- * come before any capture.  Every call shares
+ * a device looks up that array's device address (cudaGetSymbolAddress) and
+ * keeps it per device context: after the device's primary context is reset
+ * (cudaDeviceReset), the next call looks it up again.  Every call shares
  * the array, so calls whose executions overlap on the GPU (e.g. on two
  * concurrent streams) race and give wrong results; order them.  The norm
  * agrees with zero_step's within 1e-5 relative (the partial sums are grouped
