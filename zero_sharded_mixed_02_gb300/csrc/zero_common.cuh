@@ -299,6 +299,110 @@ static __device__ __forceinline__ double block_sum(double x, double* sh)
     return r;
 }
 
+// ---- the norm's sum of squares ---------------------------------------------
+// A thread's running sum of squares: an unevaluated pair of binary32 values
+// hi + lo, kept normalised by Knuth's two-sum (about 48 significant bits, where
+// the norm's tolerance needs 24), plus a binary64 part for the groups whose
+// binary32 sum of squares would lose range.  GB300 runs binary64 at a small
+// fraction of its binary32 rate, so one binary64 add per 8 elements, and a
+// binary64 shuffle tree per block, were a measurable share of a small step.
+struct NormAcc {
+    float  hi = 0.0f, lo = 0.0f;
+    double wide = 0.0;
+};
+
+// hi + lo += x, for x >= 0 and hi >= lo >= 0 (every term is a square): the
+// two-sum of hi and x, its error folded into lo, renormalised.
+static __device__ __forceinline__ void pair_add(float& hi, float& lo, float xh, float xl)
+{
+    const float s  = __fadd_rn(hi, xh);
+    const float bb = __fsub_rn(s, hi);
+    float e = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(xh, bb));
+    e = __fadd_rn(e, __fadd_rn(lo, xl));
+    hi = __fadd_rn(s, e);
+    lo = __fsub_rn(e, __fsub_rn(hi, s));
+}
+
+// One group of 8: the binary32 FMA chain of its squares, added to the pair, or,
+// for groups whose binary32 sum would lose range (very large or very small
+// gradients), the exact binary64 chain added to the binary64 part.  An inf or
+// NaN takes the binary64 part (inf) or spreads through the pair (NaN), as it
+// would through a binary64 sum.
+static __device__ __forceinline__ void add_group(NormAcc& acc, const float (&g)[8])
+{
+    float q = 0.0f;
+    int nz = 0;
+#pragma unroll
+    for (int e = 0; e < 8; e++) {
+        q = __fmaf_rn(g[e], g[e], q);
+        nz |= (g[e] != 0.0f);
+    }
+    if ((q > 1.2676506e30f || q < 8.6736174e-19f) && nz) {   // 2^100, 2^-60
+        double d = 0.0;
+#pragma unroll
+        for (int e = 0; e < 8; e++) d = __fma_rn((double)g[e], (double)g[e], d);
+        acc.wide = __dadd_rn(acc.wide, d);
+    } else {
+        pair_add(acc.hi, acc.lo, q, 0.0f);
+    }
+}
+
+// One element (ragged tails), in the binary64 part.
+static __device__ __forceinline__ void add_one(NormAcc& acc, float g)
+{
+    acc.wide = __fma_rn((double)g, (double)g, acc.wide);
+}
+
+struct NormShared {
+    float  hi[32], lo[32];
+    double wide[32];
+    int    last;
+};
+
+static __device__ __forceinline__ bool nonzero64(double x)
+{
+    return (__double_as_longlong(x) << 1) != 0;    // integer test: no binary64 compare
+}
+
+static __device__ __forceinline__ void warp_norm(NormAcc& a)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float h = __shfl_down_sync(0xFFFFFFFFu, a.hi, o);
+        const float l = __shfl_down_sync(0xFFFFFFFFu, a.lo, o);
+        pair_add(a.hi, a.lo, h, l);
+    }
+    if (__any_sync(0xFFFFFFFFu, nonzero64(a.wide))) a.wide = warp_sum(a.wide);
+}
+
+// The block's sum of its threads' accumulators (a fixed shuffle tree: the
+// pairs always, the binary64 parts when any is non-zero), as one binary64 value
+// valid in thread 0.  Any block size up to 1024 threads.
+static __device__ __forceinline__ double block_norm(NormAcc a, NormShared& sh)
+{
+    warp_norm(a);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (l == 0) {
+        sh.hi[w] = a.hi;
+        sh.lo[w] = a.lo;
+        sh.wide[w] = a.wide;
+    }
+    __syncthreads();
+    double r = 0.0;
+    if (w == 0) {
+        NormAcc b;
+        if (l < (int)(blockDim.x >> 5)) {
+            b.hi = sh.hi[l];
+            b.lo = sh.lo[l];
+            b.wide = sh.wide[l];
+        }
+        warp_norm(b);
+        r = __dadd_rn(__dadd_rn((double)b.hi, (double)b.lo), b.wide);
+    }
+    __syncthreads();
+    return r;
+}
+
 static __device__ __forceinline__ int block_or(int f, int* sh)
 {
     f = __any_sync(0xFFFFFFFFu, f);

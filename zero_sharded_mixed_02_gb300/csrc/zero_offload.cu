@@ -31,12 +31,12 @@ template <int DT, int ND>
 __global__ void __launch_bounds__(ZERO_THREADS, 4) k_reduce16(const StepArgs a,
                                                               uint16_t* __restrict g16)
 {
-    __shared__ RedShared sh;
+    __shared__ NormShared sh;
     const int nd = ND > 0 ? ND : a.nd;
     Unscale mean, unscale;
     mean.init(nd, 1.0f);                            // fold / nd
     unscale.init(1, a.state->sc.loss_scale);        // copied value / S
-    double acc = 0.0;
+    NormAcc acc;
     int bad = 0;
     const int64_t nvec = a.n >> 3;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(ZERO_THREADS, 4) k_reduce16(const StepArgs a,
         }
 #pragma unroll
         for (int e = 0; e < 8; e++) bad |= not_finite(g[e]);
-        acc += group_sumsq(g);
+        add_group(acc, g);
         __stcs(reinterpret_cast<uint4*>(g16) + vi, make_uint4(w[0], w[1], w[2], w[3]));
     }
     if (blockIdx.x == 0 && threadIdx.x < 8) {            // the ragged tail (< 8 elements)
@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(ZERO_THREADS, 4) k_reduce16(const StepArgs a,
             const uint16_t q = narrow1<DT>(mean(fold1<DT>(a.grads, a.rank_stride, i, nd)));
             const float g = unscale(widen1<DT>(q));
             bad |= not_finite(g);
-            acc = __fma_rn((double)g, (double)g, acc);
+            add_one(acc, g);
             g16[i] = q;
         }
     }

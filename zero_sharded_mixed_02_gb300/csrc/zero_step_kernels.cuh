@@ -7,6 +7,8 @@
 // combination are the same on every run.  The last block to finish (an atomic
 // ticket, no waiting) combines the per-block partials in block order and
 // writes the step status.  The update pass uses one thread per 4 elements.
+// The sums of squares are kept as binary32 pairs up to each block's partial
+// (NormAcc, zero_common.cuh); the partials and their combination are binary64.
 #pragma once
 
 #include "zero_common.cuh"
@@ -14,9 +16,10 @@
 
 namespace zero {
 
-// Norm partial of one group of 8: an FMA chain in binary32, moved to binary64
-// per group.  Groups whose binary32 sum of squares would lose range (very large
-// or very small gradients) are summed exactly in binary64 instead.
+// Norm partial of one group of 8 for the no-allocation norm: an FMA chain in
+// binary32, moved to binary64 per group.  Groups whose binary32 sum of squares
+// would lose range (very large or very small gradients) are summed exactly in
+// binary64 instead.
 static __device__ __forceinline__ double group_sumsq(const float (&g)[8])
 {
     float q = 0.0f;
@@ -37,18 +40,19 @@ static __device__ __forceinline__ double group_sumsq(const float (&g)[8])
 
 // Scalar bookkeeping of the step (thread 0 of the last block): global norm,
 // clip coefficient, skip decision, loss-scale backoff/growth, t and the bias
-// corrections.  Binary64 operations are IEEE round-to-nearest.
-static __device__ __noinline__ void finalize(const StepArgs a, double sumsq, int overflow)
+// corrections.  sc and err: the step's scalars and sticky error word.  Binary64
+// operations are IEEE round-to-nearest.
+static __device__ __noinline__ void finalize(const StepArgs& a, DevScalars sc, int32_t err,
+                                             double sumsq, int overflow)
 {
     DevState* S = a.state;
-    DevScalars sc = S->sc;
     DevStatus st;
     st.overflow   = overflow;
     st.used_scale = sc.loss_scale;
     st.grad_norm  = __dsqrt_rn(sumsq);
     st.clip_coef  = (a.clip > 0.0f && st.grad_norm > (double)a.clip)
                         ? __double2float_rn(__ddiv_rn((double)a.clip, st.grad_norm)) : 1.0f;
-    st.err = S->st.err;        // sticky: a bounded wait that gave up, in any step
+    st.err = err;              // sticky: a bounded wait that gave up, in any step
     st.pad = 0;
     if (overflow && (a.dynamic || a.skip_static)) {
         st.skipped = 1;
@@ -85,14 +89,26 @@ struct RedShared {
     int    last;
 };
 
+// The ticket: an atomic add with release and acquire semantics at GPU scope.
+// Its release orders this thread's partial and flag stores (and, through the
+// block's barriers, its block's stores) before the increment; the last block's
+// acquire, with the barrier after it, orders every block's partial before its
+// reads.  No separate fences.
+static __device__ __forceinline__ unsigned ticket_acq_rel(unsigned* counter)
+{
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
+    return old;
+}
+
 // Publish this block's partial; the last block to arrive finalizes the step.  A
 // bucket's reduce only stores its blocks' partials: the apply step combines every
 // bucket's, so a bucket's grid ends with its last block's store.
-static __device__ __forceinline__ void reduce_and_finalize(const StepArgs& a, double acc, int bad,
-                                                    RedShared& sh)
+static __device__ __forceinline__ void reduce_and_finalize(const StepArgs& a, const NormAcc& acc,
+                                                           int bad, NormShared& sh)
 {
-    const double bsum = block_sum(acc, sh.d);
-    const int    bbad = block_or(bad, sh.i);
+    const double bsum = block_norm(acc, sh);
+    const int    bbad = __syncthreads_or(bad);
     if (a.bucket >= 0) {
         if (threadIdx.x == 0) {
             a.bucket_partial[blockIdx.x] = bsum;
@@ -103,23 +119,24 @@ static __device__ __forceinline__ void reduce_and_finalize(const StepArgs& a, do
     if (threadIdx.x == 0) {
         a.state->partial[blockIdx.x] = bsum;
         a.state->flag[blockIdx.x]    = bbad;
-        __threadfence();
-        const unsigned ticket = atomicAdd(&a.state->counter, 1u);
-        sh.last = (ticket == gridDim.x - 1);
+        sh.last = (ticket_acq_rel(&a.state->counter) == gridDim.x - 1);
     }
     __syncthreads();
     if (!sh.last) return;
-    __threadfence();
+    // thread 0's acquire (the ticket) and the barrier order every block's
+    // partial before these reads
     double x = 0.0;
     int f = 0;
     for (int b = threadIdx.x; b < (int)gridDim.x; b += blockDim.x) {
-        x += __ldcg(&a.state->partial[b]);
+        x = __dadd_rn(x, __ldcg(&a.state->partial[b]));
         f |= __ldcg(&a.state->flag[b]);
     }
-    const double total = block_sum(x, sh.d);
-    const int    any   = block_or(f, sh.i);
+    NormAcc xa;
+    xa.wide = x;
+    const double total = block_norm(xa, sh);
+    const int    any   = __syncthreads_or(f);
     if (threadIdx.x == 0) {
-        finalize(a, total, any);
+        finalize(a, a.state->sc, a.state->st.err, total, any);
         a.state->counter = 0;
     }
 }
@@ -134,18 +151,18 @@ template <int DT>
 __global__ void __launch_bounds__(ZERO_THREADS) k_bucket_finalize(const StepArgs a, int nbuckets,
                                                                   int grid, int last_grid)
 {
-    __shared__ RedShared sh;
+    __shared__ NormShared sh;
     const int F = gridDim.x;
     const int b0 = (int)((int64_t)nbuckets * blockIdx.x / F);
     const int b1 = (int)((int64_t)nbuckets * (blockIdx.x + 1) / F);
-    double x = 0.0;
+    NormAcc x;
     int f = 0;
     for (int b = b0; b < b1; b++) {
         const int slots = b == nbuckets - 1 ? last_grid : grid;
         const double* p = a.bucket_partial + (int64_t)b * grid;
         const int32_t* q = a.bucket_flag + (int64_t)b * grid;
         for (int s = threadIdx.x; s < slots; s += blockDim.x) {
-            x += p[s];
+            x.wide = __dadd_rn(x.wide, p[s]);
             f |= q[s];
         }
     }
@@ -164,7 +181,7 @@ static __device__ __forceinline__ void unpack8(const float4 a, const float4 b, f
 template <int DT, int ND, bool WRITE_G>
 __global__ void __launch_bounds__(ZERO_THREADS, 4) k_reduce(const StepArgs a)
 {
-    __shared__ RedShared sh;
+    __shared__ NormShared sh;
     // the update pass may be scheduled now: it loads its state, then waits for
     // this grid to finish before it reads anything this grid writes
     asm volatile("griddepcontrol.launch_dependents;");
@@ -176,7 +193,7 @@ __global__ void __launch_bounds__(ZERO_THREADS, 4) k_reduce(const StepArgs a)
     const int nd = ND > 0 ? ND : a.nd;
     Unscale un;
     un.init(nd, a.state->sc.loss_scale);
-    double acc = 0.0;
+    NormAcc acc;
     int bad = 0;
     const int64_t nvec = a.n >> 3;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -188,7 +205,7 @@ __global__ void __launch_bounds__(ZERO_THREADS, 4) k_reduce(const StepArgs a)
             g[e] = un(s[e]);
             bad |= not_finite(g[e]);
         }
-        acc += group_sumsq(g);
+        add_group(acc, g);
         if (WRITE_G) {
             float4* o = reinterpret_cast<float4*>(a.g32) + 2 * vi;
             __stcs(o, make_float4(g[0], g[1], g[2], g[3]));
@@ -200,7 +217,7 @@ __global__ void __launch_bounds__(ZERO_THREADS, 4) k_reduce(const StepArgs a)
         if (i < a.n) {
             const float g = un(fold1<DT>(a.grads, a.rank_stride, i, nd));
             bad |= not_finite(g);
-            acc = __fma_rn((double)g, (double)g, acc);
+            add_one(acc, g);
             if (WRITE_G) a.g32[i] = g;
         }
     }
@@ -361,7 +378,7 @@ __global__ void __launch_bounds__(ZERO_THREADS) k_update(const StepArgs a)
 template <int DT, int ND, bool PP = false>
 static __device__ __forceinline__ void fused8(const StepArgs& a, int64_t vi, int nd,
                                               const Unscale& un, float bc1, float bc2,
-                                              double& acc, int& bad, uint4& w, int cur = 0)
+                                              NormAcc& acc, int& bad, uint4& w, int cur = 0)
 {
     float4* pm = reinterpret_cast<float4*>(a.master);
     float4* mm = reinterpret_cast<float4*>(a.m);
@@ -390,7 +407,7 @@ static __device__ __forceinline__ void fused8(const StepArgs& a, int64_t vi, int
         g[e] = un(s[e]);
         bad |= not_finite(g[e]);
     }
-    acc += group_sumsq(g);
+    add_group(acc, g);
     unpack8(p0, p1, p);
     unpack8(m0, m1, m);
     unpack8(v0, v1, v);
@@ -417,7 +434,7 @@ static __device__ __forceinline__ void fused8(const StepArgs& a, int64_t vi, int
 template <int DT, int ND, int QB, bool PP = false>
 static __device__ __forceinline__ void fused_pass(const StepArgs& a)
 {
-    __shared__ RedShared sh;
+    __shared__ NormShared sh;
     if constexpr (PP) asm volatile("griddepcontrol.launch_dependents;");
     const DevScalars sc = a.state->sc;
     const int nd = ND > 0 ? ND : a.nd;
@@ -425,7 +442,7 @@ static __device__ __forceinline__ void fused_pass(const StepArgs& a)
     un.init(nd, sc.loss_scale);
     // bias corrections of step t+1 (this path never skips), kept by the last step
     const float bc1 = sc.bc1_next, bc2 = sc.bc2_next;
-    double acc = 0.0;
+    NormAcc acc;
     int bad = 0;
     const int64_t nvec = a.n >> 3;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -456,7 +473,7 @@ static __device__ __forceinline__ void fused_pass(const StepArgs& a)
         if (i < a.n) {
             const float g = un(fold1<DT>(a.grads, a.rank_stride, i, nd));
             bad |= not_finite(g);
-            acc = __fma_rn((double)g, (double)g, acc);
+            add_one(acc, g);
             float* pi = a.master;
             float* mi = a.m;
             float* vi1 = a.v;
@@ -481,8 +498,10 @@ static __device__ __forceinline__ void fused_pass(const StepArgs& a)
     reduce_and_finalize(a, acc, bad, sh);
 }
 
+// Held to 4 blocks per SM (2 for the generic rank count), which every
+// compiled-in rank count reaches without spilling.
 template <int DT, int ND>
-__global__ void __launch_bounds__(ZERO_THREADS) k_fused(const StepArgs a)
+__global__ void __launch_bounds__(ZERO_THREADS, ND == 0 ? 2 : 4) k_fused(const StepArgs a)
 {
     fused_pass<DT, ND, 0>(a);
 }

@@ -81,39 +81,9 @@ static __device__ __forceinline__ int wait_bounded(uint32_t bar, uint32_t parity
 struct TmaShared {
     uint64_t full[ZERO_TMA_MAX_STAGES];
     uint64_t empty[ZERO_TMA_MAX_STAGES];
-    double d[ZERO_TMA_THREADS / 32];
-    int i[ZERO_TMA_THREADS / 32];
-    int last;
+    NormShared norm;
     int abort_flag;
 };
-
-static __device__ __forceinline__ double block_sum_w(double x, double* sh)
-{
-    x = warp_sum(x);
-    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    if (l == 0) sh[w] = x;
-    __syncthreads();
-    double r = 0.0;
-    if (w == 0) {
-        r = (l < (int)(blockDim.x >> 5)) ? sh[l] : 0.0;
-        r = warp_sum(r);
-    }
-    __syncthreads();
-    return r;
-}
-
-static __device__ __forceinline__ int block_or_w(int f, int* sh)
-{
-    f = __any_sync(0xFFFFFFFFu, f);
-    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    if (l == 0) sh[w] = f;
-    __syncthreads();
-    int r = 0;
-    if (threadIdx.x == 0)
-        for (int k = 0; k < (int)(blockDim.x >> 5); k++) r |= sh[k];
-    __syncthreads();
-    return r;
-}
 
 // Stage count for nd rank rows of 2 KB: about 128 KB of staged rows, 2..8 stages.
 __host__ __device__ constexpr int tma_stages_for(int nd)
@@ -149,7 +119,7 @@ __global__ void __launch_bounds__(ZERO_TMA_THREADS, 1) k_reduce_tma(const StepAr
         fence_mbar_init();
     }
     __syncthreads();
-    double acc = 0.0;
+    NormAcc acc;
     int bad = 0;
     int64_t issued = 0;                                     // tiles the producer issued
     if (warp == 8) {                                        // producer
@@ -216,14 +186,14 @@ __global__ void __launch_bounds__(ZERO_TMA_THREADS, 1) k_reduce_tma(const StepAr
                 bad |= not_finite(g[e]);
                 g[4 + e] = 0.0f;
             }
-            acc += group_sumsq(g);
+            add_group(acc, g);
             __stcs(reinterpret_cast<float4*>(a.g32 + base) + t, make_float4(g[0], g[1], g[2], g[3]));
         }
         if (blockIdx.x == gridDim.x - 1 && !*(volatile int*)&sh.abort_flag) {   // ragged remainder
             for (int64_t i = ntiles * ZERO_TMA_TILE + t; i < a.n; i += 256) {
                 const float g = un(fold1<DT>(a.grads, a.rank_stride, i, nd));
                 bad |= not_finite(g);
-                acc = __fma_rn((double)g, (double)g, acc);
+                add_one(acc, g);
                 a.g32[i] = g;
             }
         }
@@ -242,29 +212,7 @@ __global__ void __launch_bounds__(ZERO_TMA_THREADS, 1) k_reduce_tma(const StepAr
                                                  (uint32_t)((k / stages) & 1));
                  it++) {
             }
-    const double bsum = block_sum_w(acc, sh.d);
-    const int bbad = block_or_w(bad, sh.i);
-    if (threadIdx.x == 0) {
-        a.state->partial[blockIdx.x] = bsum;
-        a.state->flag[blockIdx.x] = bbad;
-        __threadfence();
-        sh.last = (atomicAdd(&a.state->counter, 1u) == gridDim.x - 1);
-    }
-    __syncthreads();
-    if (!sh.last) return;
-    __threadfence();
-    double x = 0.0;
-    int f = 0;
-    for (int b = threadIdx.x; b < (int)gridDim.x; b += blockDim.x) {
-        x += __ldcg(&a.state->partial[b]);
-        f |= __ldcg(&a.state->flag[b]);
-    }
-    const double total = block_sum_w(x, sh.d);
-    const int any = block_or_w(f, sh.i);
-    if (threadIdx.x == 0) {
-        finalize(a, total, any);
-        a.state->counter = 0;
-    }
+    reduce_and_finalize(a, acc, bad, sh.norm);
 }
 
 }  // namespace zero
