@@ -194,6 +194,31 @@ def test_static_scale_overflow_against_the_oracle(z, name):
         assert bad.sum() == 2                      # the two planted elements only
 
 
+NORM_RANGE = {
+    # name: case settings.  The per-group binary32 sum of squares q of 8 averaged
+    # gradients goes to the thread's binary32 pair when 2^-60 <= q <= 2^100 and to
+    # its binary64 part otherwise; sigma puts the groups across a boundary (both
+    # parts in use in every block) or wholly past it.
+    "edge-high": dict(grad_sigma=8.3e14, clip=1.0),
+    "edge-low": dict(grad_sigma=6.9e-10, clip=1e-8),
+    "past-high": dict(grad_sigma=1e20, clip=1.0),
+    "past-low": dict(grad_sigma=1e-25, clip=1e-30),
+    "edge-low-no-clip": dict(grad_sigma=6.9e-10),
+}
+
+
+@pytest.mark.parametrize("name", sorted(NORM_RANGE))
+def test_norm_across_binary32_range(z, name):
+    """bf16 gradients whose squares leave binary32's comfortable range: the norm
+    against the oracle's binary64 sum (within the harness's bound; the clip
+    coefficient it gives admitted within 8 ulp), and the state bit for bit."""
+    c = H.Case(shapes=[(40_000,), (1_003,)], nd=4, steps=3, dtype=gen.BF16, **NORM_RANGE[name])
+    gpu, ora = check(z, c)
+    assert all(np.isfinite(r["grad_norm"]) and r["grad_norm"] > 0 for r in gpu.results)
+    if c.clip:
+        assert all(r["clip_coef"] < 1.0 for r in gpu.results)
+
+
 def test_empty_model(z):
     plan = z.zero_plan_create(0, 4, 2, 1, [], z.hparams())
     try:
