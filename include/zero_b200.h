@@ -191,6 +191,11 @@ zero_status_t zero_plan_unit(zero_plan_t plan, int unit, uint64_t* len, uint64_t
  *              cover the resident shard (the scalar all-reduce over ranks has
  *              a single participant here).
  * workspace: zero_plan_layout's workspace_bytes of device scratch (NULL when 0).
+ * grads may also lie in page-locked host memory that the device can address
+ * (cudaHostAlloc, or cudaHostRegister; under unified addressing the host address
+ * is the device address): the passes then read it in place over the host link,
+ * with the same results; the caller must not rewrite it before the step is done
+ * (zero_step_result waits for it).  Every other buffer is device memory.
  * On a skipped step nothing but the plan's loss scale changes.
  * Errors: ZERO_EINVAL (null or misaligned pointer), ZERO_ECUDA. */
 zero_status_t zero_step(zero_plan_t plan, const void* grads, float* master, float* m, float* v,

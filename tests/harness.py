@@ -220,7 +220,11 @@ def stage3_valid_mask(z, plan, nd, rank=0):
     return mask
 
 
-def run_gpu(z, c: Case, keep_g32=False, plan_out=None, reduce_kernel=0) -> Run:
+def run_gpu(z, c: Case, keep_g32=False, plan_out=None, reduce_kernel=0,
+            grads_on_host=False) -> Run:
+    """The case through zero_step.  grads_on_host: the ranks' gradients stay in
+    page-locked host memory (cudaHostAlloc, mapped into the device's address
+    space) and the step reads them there."""
     import torch
     dev = torch.device("cuda", 0)
     plan = z.zero_plan_create(c.psi, c.nd, c.stage, c.dtype, c.shapes, c.hparams(z),
@@ -240,7 +244,10 @@ def run_gpu(z, c: Case, keep_g32=False, plan_out=None, reduce_kernel=0) -> Run:
         v = torch.zeros(padded, dtype=torch.float32, device=dev)
         params = torch.zeros(padded, dtype=torch.int16, device=dev)
         work = torch.empty(max(ws, 16) // 4, dtype=torch.float32, device=dev) if ws else None
-        grads = torch.empty((c.nd, padded), dtype=torch.int16, device=dev)
+        if grads_on_host:
+            grads = torch.empty((c.nd, padded), dtype=torch.int16, pin_memory=True)
+        else:
+            grads = torch.empty((c.nd, padded), dtype=torch.int16, device=dev)
         stream = torch.cuda.current_stream().cuda_stream
         results = []
         scale = c.loss_scale

@@ -219,6 +219,35 @@ def test_norm_across_binary32_range(z, name):
         assert all(r["clip_coef"] < 1.0 for r in gpu.results)
 
 
+HOST_GRADS = {
+    # name: (case settings, kernel path)
+    "two-pass-clip": (dict(shapes=[(300_001,), (77,)], nd=16, dtype=gen.FP16, grad_sigma=1e-3,
+                           loss_scale=4096.0, dynamic_scale=1, clip=0.5, inf_steps=(2,)), 1),
+    "fused": (dict(shapes=[(200_003,)], nd=8), 0),
+    "recompute": (dict(shapes=[(200_003,)], nd=2, clip=1.0), 2),
+    "stage3": (dict(shapes=[(5000,), (77,), (3000, 3)], units=[0, 0, 1], nd=8, stage=3,
+                    clip=1.0), 1),
+}
+
+
+@pytest.mark.parametrize("name", sorted(HOST_GRADS))
+def test_grads_in_page_locked_host_memory(z, name):
+    """zero_step given the ranks' gradients in page-locked host memory (read in
+    place over the host link) leaves the state and reports the results of the
+    same steps from device memory, bit for bit."""
+    over, path = HOST_GRADS[name]
+    c = H.Case(steps=4, **over)
+    plan = z.zero_plan_create(c.psi, c.nd, c.stage, c.dtype, c.shapes, c.hparams(z),
+                              units=c.units if c.stage == 3 else None)
+    assert z.zero_plan_path(plan) == path
+    z.zero_plan_destroy(plan)
+    a = H.run_gpu(z, c)
+    b = H.run_gpu(z, c, grads_on_host=True)
+    assert a.results == b.results
+    for x, y in zip((a.master, a.m, a.v, a.params), (b.master, b.m, b.v, b.params)):
+        assert x.tobytes() == y.tobytes()
+
+
 def test_empty_model(z):
     plan = z.zero_plan_create(0, 4, 2, 1, [], z.hparams())
     try:
